@@ -1,0 +1,20 @@
+"""GB300 (sm_103a) fused attention forward: prefill, split-KV decode, paged decode.
+
+The computation runs in the CUDA library ``libfa_gb300.so`` (C ABI in
+``include/fa_gb300.h``); ``api`` holds thin PyTorch-facing wrappers with the
+same names, ``costmodel`` the FLOP and byte accounting used for rooflines.
+"""
+
+from .api import (  # noqa: F401
+    FAError,
+    fa_decode_paged,
+    fa_decode_splitkv,
+    fa_decode_workspace_bytes,
+    fa_fwd,
+    fa_fwd_f32,
+    fa_get_last_device_error,
+    fa_lse_merge,
+    fa_num_splits_heuristic,
+    fa_selftest_wait_timeout,
+    fa_set_wait_timeout_ns,
+)

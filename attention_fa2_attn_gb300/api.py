@@ -1,0 +1,178 @@
+"""PyTorch-facing calls with the same names as the C ABI.
+
+Argument marshalling only: shapes are read from the tensors, output and
+workspace tensors are allocated with torch, and the call goes through the C
+library on the tensors' current CUDA stream. Every step of the attention runs
+in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from ._lib import FAError, check, lib
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, want_lse: bool = True):
+    """Prefill forward: q [B][Hq][T][d], k, v [B][Hkv][S][d] bf16 -> (o bf16, lse fp32 or None)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Hq, T, d = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale, int(causal), _stream(q))
+    check(st, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_f32(q, k, v, causal: bool = False, scale: float | None = None):
+    """The same forward in fp32 on the CUDA cores: fp32 q, k, v -> (o fp32, lse fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.float32, 4)
+    B, Hq, T, d = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    st = lib().fa_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale, int(causal), _stream(q))
+    check(st, "fa_fwd_f32")
+    return o, lse
+
+
+def fa_num_splits_heuristic(B: int, Hkv: int, S: int, num_sms: int) -> int:
+    return int(lib().fa_num_splits_heuristic(B, Hkv, S, num_sms))
+
+
+def fa_decode_workspace_bytes(B: int, Hq: int, T: int, d: int, num_splits: int) -> int:
+    return int(lib().fa_decode_workspace_bytes(B, Hq, T, d, num_splits))
+
+
+def _resolve_splits(num_splits: int, B: int, Hkv: int, S: int, device) -> int:
+    if num_splits:
+        return int(num_splits)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return fa_num_splits_heuristic(B, Hkv, S, sms)
+
+
+def _workspace(B, Hq, T, d, n, device, workspace):
+    nbytes = fa_decode_workspace_bytes(B, Hq, T, d, n)
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    return workspace, workspace.numel()
+
+
+def fa_decode_splitkv(q, k, v, causal: bool = True, num_splits: int = 0, scale: float | None = None,
+                      workspace=None, out=None, lse=None):
+    """Split-KV decode: q [B][Hq][T][d], k, v [B][Hkv][S][d] bf16 -> (o, lse)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Hq, T, d = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    n = _resolve_splits(num_splits, B, Hkv, S, q.device)
+    ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
+                                 int(causal), n, _ptr(ws), ws_bytes, _stream(q))
+    check(st, "fa_decode_splitkv")
+    return o, lse
+
+
+def fa_lse_merge(o_part, lse_part):
+    """Merge o_part [n][rows][d] fp32 and lse_part [n][rows] fp32 -> (o [rows][d] bf16, lse [rows] fp32)."""
+    _need(o_part, "o_part", torch.float32, 3)
+    _need(lse_part, "lse_part", torch.float32, 2)
+    n, rows, d = o_part.shape
+    if tuple(lse_part.shape) != (n, rows):
+        raise ValueError("lse_part must be [n][rows]")
+    o = torch.empty((rows, d), dtype=torch.bfloat16, device=o_part.device)
+    lse = torch.empty((rows,), dtype=torch.float32, device=o_part.device)
+    st = lib().fa_lse_merge(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), n, rows, d, _stream(o_part))
+    check(st, "fa_lse_merge")
+    return o, lse
+
+
+def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = True, num_splits: int = 1,
+                    scale: float | None = None, workspace=None, out=None, lse=None):
+    """Paged decode: pools [P][16][Hkv][d] bf16, block_table [B][max_pages] int32, seqlens [B] int32."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    B, Hq, T, d = q.shape
+    P, page_size, Hkv, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    n = _resolve_splits(num_splits, B, Hkv, max_pages * page_size, q.device)
+    ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), _ptr(o),
+                               _ptr(lse), B, Hq, Hkv, T, max_pages, page_size, P, d, scale, int(causal), n, _ptr(ws),
+                               ws_bytes, _stream(q))
+    check(st, "fa_decode_paged")
+    return o, lse
+
+
+def fa_get_last_device_error(device=None) -> tuple[int, int]:
+    """Synchronise the current stream and read/clear the device error word -> (status, raw word)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    detail = ctypes.c_int(0)
+    st = lib().fa_get_last_device_error(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream), ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    lib().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_selftest_wait_timeout(timeout_ns: int, device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = lib().fa_selftest_wait_timeout(int(timeout_ns), ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    check(st, "fa_selftest_wait_timeout")
+
+
+__all__ = [
+    "FAError",
+    "fa_fwd",
+    "fa_fwd_f32",
+    "fa_num_splits_heuristic",
+    "fa_decode_workspace_bytes",
+    "fa_decode_splitkv",
+    "fa_lse_merge",
+    "fa_decode_paged",
+    "fa_get_last_device_error",
+    "fa_set_wait_timeout_ns",
+    "fa_selftest_wait_timeout",
+]

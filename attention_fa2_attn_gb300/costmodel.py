@@ -1,0 +1,88 @@
+"""FLOP and byte accounting for the roofline numbers.
+
+Formulas restated from the pages:
+  * "Softmax and FlashAttention", section "Maths" (HBM traffic): standard
+    attention moves e(2Nd + 4N^2 + 2Nd) bytes; FlashAttention-2 moves
+    e(2Nd + 2N^2 d / Br) with no L2 reuse and 4eNd at the floor, e bytes per
+    value.
+  * "Attention kernel chains", "What FlashAttention removes from HBM":
+    4 N^2 d FLOPs per head (two GEMMs of 2 N^2 d), unchanged by tiling; the
+    causal convention halves it.
+  * "GQA loads KV once per group" and "The block-table cost of paged
+    attention": a decode step reads every K/V byte of its KV heads once;
+    the block table costs 4 bytes per page.
+"""
+
+from __future__ import annotations
+
+
+def attention_flops(B: int, Hq: int, T: int, S: int, d: int, causal: bool) -> float:
+    """4*T*S*d per query head (QK^T and PV), halved for causal."""
+    f = 4.0 * B * Hq * T * S * d
+    return f / 2.0 if causal else f
+
+
+def standard_attention_bytes(N: int, d: int, e: int = 2) -> float:
+    """Three-kernel attention of one head: read Q, K; write+read S; write+read P; read V; write O."""
+    return e * (2 * N * d + 4 * N * N + 2 * N * d)
+
+
+def flash2_bytes(N: int, d: int, e: int = 2, Br: int = 128) -> float:
+    """FlashAttention-2, one head, no L2 reuse: Q and O once, K and V once per query block."""
+    return e * (2 * N * d + 2 * N * N * d / Br)
+
+
+def flash2_floor_bytes(N: int, d: int, e: int = 2) -> float:
+    """Every value of Q, K, V and O moved once."""
+    return 4 * e * N * d
+
+
+def flash2_tile_bytes(N: int, d: int, e: int = 2, Br: int = 128, Bc: int = 128) -> tuple[float, float]:
+    """Per-tile counter over the (query block i, key block j) loop: (moved, once).
+
+    ``moved`` counts a Q block when its row of tiles starts and a K and V
+    block at every tile (no L2 reuse); ``once`` counts each K/V block only for
+    the first query block (every re-read hits L2). Neither includes the O write.
+    """
+    moved = once = 0.0
+    nq = -(-N // Br)
+    nk = -(-N // Bc)
+    for i in range(nq):
+        for j in range(nk):
+            if j == 0:
+                moved += e * Br * d
+                once += e * Br * d
+            moved += 2 * e * Bc * d
+            if i == 0:
+                once += 2 * e * Bc * d
+    return moved, once
+
+
+def prefill_compulsory_bytes(B: int, Hq: int, Hkv: int, T: int, S: int, d: int, e: int = 2) -> float:
+    """Q read, O written, K and V read once, fp32 lse written."""
+    return e * (2 * B * Hq * T * d + 2 * B * Hkv * S * d) + 4 * B * Hq * T
+
+
+def decode_kv_bytes(B: int, Hkv: int, S: int, d: int, e: int = 2) -> float:
+    """K and V of every KV head read once (grouped query heads share them)."""
+    return 2.0 * B * Hkv * S * d * e
+
+
+def decode_bytes(B: int, Hq: int, Hkv: int, T: int, S: int, d: int, e: int = 2, page_size: int = 0) -> float:
+    """Algorithmic bytes of one decode step: K/V once, Q read, O written, fp32 lse
+    written, and 4 bytes per block-table entry when paged."""
+    b = decode_kv_bytes(B, Hkv, S, d, e) + 2.0 * e * B * Hq * T * d + 4.0 * B * Hq * T
+    if page_size:
+        b += 4.0 * B * (-(-S // page_size))
+    return b
+
+
+def gqa_kv_read_bytes(batch: int, context: int, kv_bytes_per_token: int, tp: int, group: int, grouped: bool) -> float:
+    """KV bytes read per GPU per decode step; without grouping each query head re-reads its KV head."""
+    b = batch * context * kv_bytes_per_token / tp
+    return b if grouped else b * group
+
+
+def paged_block_bytes(page_tokens: int, kv_heads: int, d: int, e: int = 2) -> int:
+    """K and V bytes of one page across the KV heads of a layer."""
+    return page_tokens * kv_heads * d * 2 * e

@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Throughput of the fused attention forward on one GB300, printed as ONE JSON line.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one fa_fwd call over the prefill workload (batch 4, 16 heads,
+4096 x 4096, head dim 128, bf16, non-causal) with inputs resident in HBM.
+The line carries the tensor-core roofline of that kernel, the end-to-end
+number through the C ABI with host buffers, the fp64 oracle's CPU rate, the
+SM clocks sampled during the timed region, and -- in "secondary" -- the
+other workloads: causal GQA prefill (TFLOP/s) and split-KV / paged decode
+(HBM GB/s).
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the maximum time over ranks is reported.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, one
+attention plane (one batch entry, one head) of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fa_inputs as fi  # noqa: E402
+from attention_fa2_attn_gb300 import costmodel as cm  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def load_traffic():
+    """dram bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return {}
+    out = {}
+    import hashlib
+
+    for line in open(p):
+        parts = line.split()
+        if len(parts) < 4 or line.startswith("#"):
+            continue
+        kernel, src, sha, nbytes = parts[:4]
+        path = os.path.join(ROOT, "attention_fa2_attn_gb300", "csrc", src)
+        if os.path.exists(path) and hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] == sha:
+            out[kernel] = float(nbytes)
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = (
+        "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+        "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+    )
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = 0.0
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        busy = [s for s, p in zip(sm, power) if p > 200] or sm
+        return {
+            "sm_mhz": statistics.median(busy) if busy else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+            "power_w_max": max(power) if power else None,
+        }
+
+
+# --------------------------------------------------------------------------- #
+# oracle on the host cores (cpu_baseline and the reference arm)
+# --------------------------------------------------------------------------- #
+def oracle_worker(mode: str, a: float, b: float) -> None:
+    """Child process: time the oracle's three-pass attention on the prefill workload.
+
+    mode "budget": whole (batch, head) planes until ``a`` seconds have passed.
+    mode "steps":  ``int(a)`` steps, each a block of query rows of one plane
+    (rows are independent), sized so that one step takes about ``b`` seconds.
+    """
+    import numpy as np
+
+    import oracle
+
+    w = fi.PREFILL_MHA
+    q, k, v = fi.qkv(1, 1, 1, w.T, w.S, w.d, w.index)
+    q64, k64, v64 = (x.double().numpy() for x in (q, k, v))
+    times, rows_done = [], []
+    if mode == "budget":
+        t0 = time.perf_counter()
+        while True:
+            t = time.perf_counter()
+            oracle.attention_three_pass(q64, k64, v64, w.scale, w.causal)
+            times.append(time.perf_counter() - t)
+            rows_done.append(w.T)
+            if time.perf_counter() - t0 > a:
+                break
+    else:
+        n_steps, target = int(a), float(b)
+        t = time.perf_counter()
+        oracle.attention_three_pass(q64[:, :, :256], k64, v64, w.scale, w.causal)
+        per_row = (time.perf_counter() - t) / 256
+        rows = int(min(w.T, max(16, target / max(per_row, 1e-9))))
+        for i in range(n_steps):
+            r0 = (i * rows) % max(1, w.T - rows + 1)
+            t = time.perf_counter()
+            oracle.attention_three_pass(q64[:, :, r0:r0 + rows], k64, v64, w.scale, w.causal)
+            times.append(time.perf_counter() - t)
+            rows_done.append(rows)
+    flops_per_row = cm.attention_flops(1, 1, 1, w.S, w.d, w.causal)
+    print(json.dumps({"times": times, "rows": rows_done, "flops_per_row": flops_per_row,
+                      "threads": int(os.environ.get("OMP_NUM_THREADS", "1")), "numpy": np.__version__}))
+
+
+def run_oracle_child(mode: str, a: float, b: float = 0.0) -> dict:
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", mode, str(a), str(b)],
+                       capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle worker failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args, rank: int, world: int) -> int:
+    if rank != 0:
+        return 0
+    w = fi.PREFILL_MHA
+    n = args.warmup + args.steps
+    target = min(1.0, 150.0 / n)  # the whole run stays within a few minutes
+    res = run_oracle_child("steps", n, target)
+    times = res["times"][args.warmup:]
+    rows = res["rows"][args.warmup:]
+    per_step = sum(times) / len(times)
+    value = res["flops_per_row"] * sum(rows) / sum(times) / 1e12
+    cores = res["threads"]
+    sample = (f"{rows[0]} query rows of one (batch, head) plane of {w.name} ({w.S} keys, d={w.d}) per step, "
+              f"fp64 numpy three-pass oracle")
+    line = {
+        "impl": "reference",
+        "metric": "attn fwd TFLOP/s",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": 0,
+        "steps": len(times),
+        "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "S": w.S, "d": w.d,
+                   "causal": w.causal, "sample": f"{rows[0]} rows per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------- #
+# GPU arm
+# --------------------------------------------------------------------------- #
+def time_steps(torch, step, K, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(K):
+        step()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / K  # ms per step
+
+
+def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
+    out = {}
+    gen = torch.Generator(device=dev)
+
+    def rnd(shape, seed):
+        gen.manual_seed(seed)
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    # causal GQA prefill
+    w = fi.CAUSAL_GQA
+    q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)
+    k = rnd((w.B, w.Hkv, w.S, w.d), 2000 + w.index)
+    v = rnd((w.B, w.Hkv, w.S, w.d), 3000 + w.index)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.T, device=dev)
+    step = lambda: fa.fa_fwd(q, k, v, causal=True, scale=w.scale, out=o, lse=lse)  # noqa: E731
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(torch, step, steps, stream)
+    tf = cm.attention_flops(w.B, w.Hq, w.T, w.S, w.d, True) / (ms * 1e-3) / 1e12
+    out[w.name] = {"metric": "attn fwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                   "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 1}
+    del q, k, v, o, lse
+
+    # split-KV decode (decode kernel + merge)
+    w = fi.SPLITKV_DECODE
+    q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)
+    k = rnd((w.B, w.Hkv, w.S, w.d), 2000 + w.index)
+    v = rnd((w.B, w.Hkv, w.S, w.d), 3000 + w.index)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.T, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.Hq, w.T, w.d, w.num_splits), dtype=torch.uint8, device=dev)
+    step = lambda: fa.fa_decode_splitkv(q, k, v, causal=True, num_splits=w.num_splits, scale=w.scale,  # noqa: E731
+                                        workspace=ws, out=o, lse=lse)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(torch, step, steps, stream)
+    byt = cm.decode_bytes(w.B, w.Hq, w.Hkv, w.T, w.S, w.d)
+    gbs = byt / (ms * 1e-3) / 1e9
+    out[w.name] = {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+                   "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "launches_per_step": 2,
+                   "bytes_per_step": byt, "num_splits": w.num_splits}
+    del q, k, v, o, lse, ws
+
+    # paged decode
+    w = fi.PAGED_DECODE
+    max_pages = w.S // w.page_size
+    P = w.B * max_pages
+    q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)
+    kp = rnd((P, w.page_size, w.Hkv, w.d), 2000 + w.index)
+    vp = rnd((P, w.page_size, w.Hkv, w.d), 3000 + w.index)
+    cpu_gen = torch.Generator().manual_seed(4000 + w.index)
+    table = torch.randperm(P, generator=cpu_gen).view(w.B, max_pages).to(torch.int32).to(dev)
+    sl = torch.full((w.B,), w.S, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.T, device=dev)
+    step = lambda: fa.fa_decode_paged(q, kp, vp, table, sl, causal=True, num_splits=1, scale=w.scale,  # noqa: E731
+                                      out=o, lse=lse)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(torch, step, steps, stream)
+    byt = cm.decode_bytes(w.B, w.Hq, w.Hkv, w.T, w.S, w.d, page_size=w.page_size)
+    gbs = byt / (ms * 1e-3) / 1e9
+    out[w.name] = {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+                   "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "launches_per_step": 1,
+                   "bytes_per_step": byt, "num_splits": 1}
+    del q, kp, vp, table, sl, o, lse
+    torch.cuda.empty_cache()
+    return out
+
+
+def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
+    import torch
+    import torch.distributed as dist
+
+    import attention_fa2_attn_gb300 as fa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("gloo")
+    peaks, peak_src = load_peaks()
+    w = fi.PREFILL_MHA
+    stream = torch.cuda.current_stream(dev)
+
+    gen = torch.Generator(device=dev)
+
+    def rnd(shape, seed):
+        gen.manual_seed(seed)
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)
+    k = rnd((w.B, w.Hkv, w.S, w.d), 2000 + w.index)
+    v = rnd((w.B, w.Hkv, w.S, w.d), 3000 + w.index)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.T, device=dev)
+    step = lambda: fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)  # noqa: E731
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, word = fa.fa_get_last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error after warm-up: {word:#x}")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms = time_steps(torch, step, args.steps, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+
+    flops = cm.attention_flops(w.B, w.Hq, w.T, w.S, w.d, w.causal)
+    value = flops * world / (ms * 1e-3) / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12  # one prefill launch per step
+    peak = peaks["bf16_tflops"]
+    traffic = load_traffic().get("prefill_tc_kernel")
+
+    # end to end: pinned host inputs -> HBM -> kernel -> O and lse back to pinned host memory
+    qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    k_e2e = max(3, min(args.steps, 50))
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    ms_e2e_dev = time_steps(torch, e2e_step, k_e2e, stream)
+    ms_e2e = max(ms_e2e_dev, (time.perf_counter() - t0) * 1e3 / k_e2e)
+    if world > 1:
+        t = torch.tensor([ms_e2e], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t[0])
+    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    del qh, kh, vh, oh, lh
+
+    secondary = {}
+    if not args.no_secondary and rank == 0:
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+        secondary = secondary_measurements(torch, fa, dev, stream, max(5, min(args.steps, 40)), peaks)
+    st, word = fa.fa_get_last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during the bench: {word:#x}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = run_oracle_child("budget", args.cpu_seconds)
+        secs = sum(res["times"])
+        cpu = {
+            "value": res["flops_per_row"] * sum(res["rows"]) / secs / 1e12,
+            "unit": "TFLOP/s",
+            "cores": res["threads"],
+            "kind": "oracle",
+            "sample": f"{len(res['times'])} whole (batch, head) planes of {w.name} ({w.T}x{w.S}, d={w.d}) "
+                      f"through the fp64 numpy three-pass oracle, {secs:.1f} s",
+        }
+
+    if rank == 0:
+        line = {
+            "metric": "attn fwd TFLOP/s",
+            "value": value,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "S": w.S, "d": w.d,
+                       "causal": w.causal, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (Q, K, V, O: 268 MB per step)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic, "kernel": "prefill_tc_kernel<128>",
+                         "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                         else "fallback 1.9 PFLOP/s bf16 burst"},
+            "e2e": {"value": flops / (ms_e2e * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+            "secondary": secondary,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main() -> int:
+    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-worker":
+        oracle_worker(sys.argv[2], float(sys.argv[3]), float(sys.argv[4]))
+        return 0
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    return gpu_arm(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

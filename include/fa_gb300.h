@@ -1,0 +1,197 @@
+/*
+ * fa_gb300.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * Exact scaled-dot-product attention, O = softmax(scale * Q K^T) V, computed
+ * with the online-softmax recurrence so that the score matrix never reaches
+ * device memory.
+ *
+ * Sources (page title, section):
+ *   "Kernel visualization: Flash Attention 1": "Derivation" and "The tiled
+ *       version" (the per-row recurrence for the running max, sum and output).
+ *   "Softmax and FlashAttention": "Concept" (the problem: S = QK^T, P =
+ *       softmax(S), O = PV; FlashAttention-2 loop order) and "Maths"
+ *       (exactness of the online softmax).
+ *   "Attention kernel chains: tiling, the online softmax, merges and masks":
+ *       "The log-sum-exp merge", "How many splits for decode", "The causal
+ *       mask for a decode step", "What the backward pass saves" (one fp32 LSE
+ *       per query row), "GQA loads KV once per group", "The block-table cost
+ *       of paged attention".
+ *
+ * Conventions shared by every call
+ *   - Every tensor argument is a DEVICE pointer owned by the caller, dense
+ *     row-major, 16-byte aligned. The library never frees or keeps them.
+ *   - Layouts: q, o are [B][Hq][T][d]; k, v are [B][Hkv][S][d]; lse is
+ *     [B][Hq][T] fp32 (natural log of the sum of exp of the scaled scores).
+ *   - GQA: Hq % Hkv == 0; query head h reads KV head h / (Hq / Hkv).
+ *   - causal != 0 applies the bottom-right-aligned mask: query row i (of T)
+ *     sees key j iff j <= i + (S - T). A row that sees no key (T > S) gets
+ *     O = 0 and lse = -inf.
+ *   - scale must be finite and > 0 (the pages use 1/sqrt(d)).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). Argument errors are returned synchronously, before
+ *     anything is launched; FA_ERR_CUDA reports a failed launch.
+ *   - Kernels never trap. Every wait inside a kernel is bounded; a wait that
+ *     runs out, or a bounds check that fails (paged block-table entries),
+ *     records a code in a device-side error word and the kernel returns.
+ *     fa_get_last_device_error() reads and clears that word.
+ *   - The library allocates no device memory. Scratch space (split-KV
+ *     partials) is passed in by the caller as `workspace`.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, misaligned pointer, ... */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim not in {64, 128}) */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; see fa_last_cuda_error_string() */
+  FA_ERR_TIMEOUT = 4,     /* device side: a bounded wait ran out */
+  FA_ERR_BOUNDS = 5       /* device side: a block-table entry outside [0, num_pages) */
+} fa_status;
+
+/* Library version, major*10000 + minor*100 + patch. */
+FA_API int fa_version(void);
+
+/* Human-readable name of a status code (static storage). */
+FA_API const char* fa_status_string(int status);
+
+/* Text of the last CUDA error seen by this library in this thread (static storage). */
+FA_API const char* fa_last_cuda_error_string(void);
+
+/*
+ * fa_fwd -- prefill / general forward, BF16 in, BF16 O, FP32 LSE.
+ * ("Softmax and FlashAttention", "Concept": FlashAttention-2 order; "Attention
+ *  kernel chains", "What the backward pass saves": one FP32 LSE per row;
+ *  "GQA loads KV once per group": a group's query heads share each K/V tile.)
+ *   q   [B][Hq][Tq][d]  bf16      k, v [B][Hkv][Skv][d] bf16
+ *   o   [B][Hq][Tq][d]  bf16 out  lse  [B][Hq][Tq] fp32 out, may be NULL
+ *   d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16}; Tq, Skv >= 1; B*Hq*Tq < 2^31.
+ * Runs the tcgen05 tensor-core kernel (TMA ring, TMEM accumulators).
+ */
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int Tq, int Skv, int d, float scale, int causal,
+                 void* stream);
+
+/*
+ * fa_fwd_f32 -- the same operation in FP32 throughout (inputs, accumulation,
+ * output) on the CUDA cores; for checking at 1e-5 against the fp64 oracle.
+ *   q, o [B][Hq][Tq][d] fp32; k, v [B][Hkv][Skv][d] fp32; lse as fa_fwd.
+ *   1 <= d <= 128.
+ */
+FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                     int B, int Hq, int Hkv, int Tq, int Skv, int d, float scale, int causal,
+                     void* stream);
+
+/*
+ * fa_num_splits_heuristic -- how many key ranges a decode step should use.
+ * ("Attention kernel chains", "How many splits for decode": split so that
+ *  batch x KV heads x splits fills at most one wave of SMs; no split once
+ *  batch x KV heads already fills the GPU.)
+ * Returns max(1, min(num_sms / (B*Hkv), ceil(S / 256))); 1 when B*Hkv >= num_sms.
+ * Pure host arithmetic. Returns 1 for non-positive arguments.
+ */
+FA_API int fa_num_splits_heuristic(int B, int Hkv, int S, int num_sms);
+
+/*
+ * fa_decode_workspace_bytes -- bytes of `workspace` a split decode needs:
+ * FP32 partial outputs [num_splits][B*Hq*T][d] followed (256-byte aligned) by
+ * FP32 partial lse [num_splits][B*Hq*T]. 0 when num_splits <= 1.
+ */
+FA_API size_t fa_decode_workspace_bytes(int B, int Hq, int T, int d, int num_splits);
+
+/*
+ * fa_decode_splitkv -- attention of T new queries over S contiguous cached
+ * keys, split into num_splits contiguous key ranges of ceil(S / num_splits)
+ * keys, each processed by its own CTAs, then merged by fa_lse_merge on the
+ * same stream. ("Attention kernel chains", "The log-sum-exp merge" and "How
+ * many splits for decode".)
+ *   q [B][Hq][T][d] bf16; k, v [B][Hkv][S][d] bf16; o [B][Hq][T][d] bf16 out;
+ *   lse [B][Hq][T] fp32 out (may be NULL).
+ *   d in {64, 128}; (Hq / Hkv) * T <= 16.
+ *   num_splits: 0 = fa_num_splits_heuristic(B, Hkv, S, SM count); else 1..1024.
+ *   workspace: device scratch of at least fa_decode_workspace_bytes(...)
+ *   bytes, 256-byte aligned (may be NULL when the split count is 1).
+ *   Returns FA_ERR_INVALID_ARG if ws_bytes is too small.
+ */
+FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int T, int S, int d, float scale, int causal,
+                            int num_splits, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * fa_lse_merge -- merge normalised partial results of `num_splits` key ranges.
+ * ("Attention kernel chains", "The log-sum-exp merge": lse = ln sum_s e^{lse_s},
+ *  O = sum_s e^{lse_s - lse} O_s.)
+ *   o_part   [num_splits][rows][d] fp32   lse_part [num_splits][rows] fp32
+ *   o        [rows][d] bf16 out           lse      [rows] fp32 out (may be NULL)
+ *   A split with lse_s = -inf has weight 0; a row whose splits are all -inf
+ *   gets O = 0 and lse = -inf. 1 <= d <= 256, num_splits >= 1.
+ */
+FA_API fa_status fa_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                       int num_splits, int rows, int d, void* stream);
+
+/*
+ * fa_decode_paged -- decode over a paged K/V cache.
+ * ("Attention kernel chains", "The block-table cost of paged attention":
+ *  token t of sequence b lives in slot t % page_size of pool page
+ *  block_table[b][t / page_size]; K and V share the table.)
+ *   q           [B][Hq][T][d] bf16
+ *   k_pages,
+ *   v_pages     [num_pages][page_size][Hkv][d] bf16
+ *   block_table [B][max_pages] int32 (device)
+ *   seqlens     [B] int32 (device): keys of each sequence, each in [0, max_pages*page_size]
+ *   o, lse      as fa_decode_splitkv
+ *   page_size == 16; d in {64, 128}; (Hq / Hkv) * T <= 16.
+ *   Each sequence's keys are split into num_splits ranges (0 = heuristic on
+ *   max_pages*page_size); workspace as fa_decode_splitkv.
+ *   A table entry outside [0, num_pages) is not dereferenced: the kernel
+ *   records FA_ERR_BOUNDS (read it with fa_get_last_device_error) and that
+ *   sequence's output is undefined.
+ */
+FA_API fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                          const int* block_table, const int* seqlens, void* o, float* lse,
+                          int B, int Hq, int Hkv, int T, int max_pages, int page_size,
+                          int num_pages, int d, float scale, int causal, int num_splits,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * fa_get_last_device_error -- synchronise `stream`, read and clear the
+ * device-side error word. Returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_BOUNDS
+ * (or FA_ERR_CUDA if the read itself fails). *detail (may be NULL) receives
+ * the raw word: code | site << 8.
+ */
+FA_API fa_status fa_get_last_device_error(void* stream, int* detail);
+
+/*
+ * fa_set_wait_timeout_ns -- bound, in nanoseconds of %globaltimer, for every
+ * wait inside the kernels launched after this call (default 4e9 = 4 s).
+ */
+FA_API void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * fa_selftest_wait_timeout -- failure-detection self test (no counterpart on
+ * the pages). Launches one CTA that waits, through the same bounded wait the
+ * attention kernels use, on an mbarrier that nothing ever arrives on, with a
+ * limit of `timeout_ns`. The wait must run out: the kernel records
+ * FA_ERR_TIMEOUT in the device error word and returns, leaving the context
+ * usable. Read the outcome with fa_get_last_device_error().
+ */
+FA_API fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

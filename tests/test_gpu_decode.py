@@ -1,0 +1,159 @@
+"""Parity of split-KV decode, the LSE merge and paged decode with the fp64 oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs as fi
+import oracle
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def _fa():
+    import attention_fa2_attn_gb300 as fa
+
+    return fa
+
+
+SPLIT_CASES = [
+    # B, Hq, Hkv, T, S, d, causal, splits
+    (2, 8, 2, 1, 1000, 128, True, 1),
+    (2, 8, 2, 1, 1000, 128, True, 3),
+    (2, 8, 2, 1, 1000, 128, True, 16),
+    (1, 32, 8, 1, 4097, 128, True, 0),
+    (1, 8, 1, 2, 777, 64, True, 5),  # two new queries per head: 16 stacked rows
+    (3, 4, 4, 1, 130, 64, False, 2),
+    (1, 16, 2, 2, 300, 128, True, 64),  # more splits than 64-key tiles: empty splits
+    (1, 4, 1, 3, 2, 128, True, 2),  # T > S: the first row sees no key
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "B{}_Hq{}_Hkv{}_T{}_S{}_d{}_{}_n{}".format(*c[:6], "causal" if c[6] else "full", c[7]))
+def test_splitkv_small(case):
+    B, Hq, Hkv, T, S, d, causal, n = case
+    q, k, v = fi.qkv(B, Hq, Hkv, T, S, d, 60 + S % 11)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, causal)
+    o, l = _fa().fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, num_splits=n, scale=scale)
+    compare(o, l, o_ref, l_ref, what=str(case))
+
+
+def test_splitkv_full_size():
+    w = fi.SPLITKV_DECODE
+    q, k, v = fi.qkv(w.B, w.Hq, w.Hkv, w.T, w.S, w.d, w.index)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, w.scale, w.causal)
+    o, l = _fa().fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=w.causal, num_splits=w.num_splits, scale=w.scale)
+    compare(o, l, o_ref, l_ref, what=w.name)
+    # the split count does not change the result beyond rounding ("any split is exact")
+    o1, l1 = _fa().fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=w.causal, num_splits=1, scale=w.scale)
+    compare(o1, l1, o_ref, l_ref, what=w.name + " unsplit")
+
+
+def test_merge_worked_example():
+    """Partials of the scores [1, 2] | [3] with V = identity rows merge to the
+    page's numbers: lse 3.408, weights 0.335 and 0.665."""
+    q, k, vv = np.zeros((1, 1, 1, 3)), np.zeros((1, 1, 3, 3)), np.eye(3).reshape(1, 1, 3, 3)
+    q[0, 0, 0, 0] = 1.0
+    k[0, 0, :, 0] = [1.0, 2.0, 3.0]
+    op, lp = oracle.attention_partials(q, k, vv, 1.0, False, 2)
+    o_part = torch.tensor(op.reshape(2, 1, 3), dtype=torch.float32, device=DEV)
+    lse_part = torch.tensor(lp.reshape(2, 1), dtype=torch.float32, device=DEV)
+    o, l = _fa().fa_lse_merge(o_part, lse_part)
+    assert abs(float(l[0]) - 3.408) < 5e-4
+    got = o[0].float().cpu().numpy()
+    assert abs(got[0] + got[1] - 0.335) < 5e-3 and abs(got[2] - 0.665) < 5e-3
+
+
+def test_merge_random_with_empty_splits():
+    g = torch.Generator().manual_seed(3)
+    n, rows, d = 7, 50, 128
+    o_part = torch.randn(n, rows, d, generator=g)
+    lse_part = torch.randn(n, rows, generator=g) * 5
+    lse_part[2] = -math.inf  # an empty split
+    lse_part[:, 7] = -math.inf  # a row that saw no key at all
+    o_ref, l_ref = oracle.lse_merge(o_part.numpy(), lse_part.numpy())
+    o, l = _fa().fa_lse_merge(o_part.to(DEV), lse_part.to(DEV))
+    compare(o, l, o_ref, l_ref, what="merge")
+
+
+def _paged_problem(B, Hq, Hkv, T, d, seqlens, max_pages, index):
+    k_pages, v_pages, table, _ = fi.paged_kv(B, Hkv, max_pages * 16, d, 16, index)
+    q = fi.decode_q(B, Hq, T, d, index)
+    sl = torch.tensor(seqlens, dtype=torch.int32)
+    return q, k_pages, v_pages, table, sl
+
+
+PAGED_CASES = [
+    # B, Hq, Hkv, T, d, seqlens, max_pages, splits
+    (3, 8, 2, 1, 128, [40, 16, 1], 3, 1),
+    (3, 8, 2, 1, 128, [40, 16, 1], 3, 2),
+    (4, 16, 2, 1, 64, [1000, 333, 64, 0], 64, 3),
+    (2, 8, 1, 2, 128, [517, 260], 40, 1),
+    (2, 64, 8, 1, 128, [2048, 1500], 128, 4),
+]
+
+
+@pytest.mark.parametrize("case", PAGED_CASES, ids=lambda c: "B{}_Hq{}_Hkv{}_T{}_d{}_n{}".format(*c[:5], c[7]))
+def test_paged_small(case):
+    B, Hq, Hkv, T, d, seqlens, max_pages, n = case
+    q, kp, vp, table, sl = _paged_problem(B, Hq, Hkv, T, d, seqlens, max_pages, 70 + B)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, l_ref = oracle.decode_paged(q, kp, vp, table, sl, 16, scale, True)
+    o, l = _fa().fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV), causal=True,
+                                 num_splits=n, scale=scale)
+    compare(o, l, o_ref, l_ref, what=str(case))
+
+
+def test_paged_equals_contiguous_bit_exact():
+    """Gathering the pages into contiguous K/V and running the split-KV path on
+    them gives the same bits: the block-table gather is exact."""
+    B, Hq, Hkv, T, d, S = 3, 32, 8, 1, 128, 1024
+    q, kp, vp, table, _ = _paged_problem(B, Hq, Hkv, T, d, [S] * B, S // 16, 81)
+    sl = torch.full((B,), S, dtype=torch.int32)
+    kc = torch.stack([torch.from_numpy(oracle.paged_gather(kp.float(), table[b], S, 16)) for b in range(B)]).bfloat16()
+    vc = torch.stack([torch.from_numpy(oracle.paged_gather(vp.float(), table[b], S, 16)) for b in range(B)]).bfloat16()
+    for n in (1, 3):
+        o1, l1 = _fa().fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV), num_splits=n)
+        o2, l2 = _fa().fa_decode_splitkv(q.to(DEV), kc.to(DEV), vc.to(DEV), num_splits=n)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2), n
+
+
+def test_paged_full_size():
+    w = fi.PAGED_DECODE
+    kp, vp, table, sl = fi.paged_kv(w.B, w.Hkv, w.S, w.d, w.page_size, w.index)
+    q = fi.decode_q(w.B, w.Hq, w.T, w.d, w.index)
+    o, l = _fa().fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV), causal=True,
+                                 num_splits=1, scale=w.scale)
+    o_ref, l_ref = oracle.decode_paged(q, kp, vp, table, sl, 16, w.scale, True)
+    compare(o, l, o_ref, l_ref, what=w.name)
+
+
+def test_paged_bad_table_entry_is_reported():
+    """A block-table entry outside the pool is never dereferenced: the kernel's
+    bounds check records FA_ERR_BOUNDS and the call returns normally."""
+    fa = _fa()
+    B, Hq, Hkv, T, d = 2, 8, 2, 1, 128
+    q, kp, vp, table, sl = _paged_problem(B, Hq, Hkv, T, d, [64, 64], 4, 83)
+    bad = table.clone()
+    bad[1, 2] = kp.shape[0] + 5
+    assert fa.fa_get_last_device_error()[0] == 0
+    fa.fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), bad.to(DEV), sl.to(DEV), num_splits=1)
+    st, word = fa.fa_get_last_device_error()
+    assert st == 5 and (word & 0xFF) == 5
+    # sequence 0 did not touch the bad entry and is still exact
+    o, l = fa.fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV), num_splits=1)
+    o_ref, l_ref = oracle.decode_paged(q, kp, vp, table, sl, 16, 1 / math.sqrt(d), True)
+    compare(o, l, o_ref, l_ref, what="after bounds error")
+    assert fa.fa_get_last_device_error()[0] == 0

@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+checks reject bad arguments before anything is launched (CPU only: no call
+here reaches a CUDA API)."""
+
+import ctypes
+import json
+import os
+
+import pytest
+
+from attention_fa2_attn_gb300 import _lib
+
+G = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_worked_examples.json")))
+P = ctypes.c_void_p(256)  # a fake, aligned, non-null "device pointer": never dereferenced here
+MIS = ctypes.c_void_p(258)  # misaligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    return _lib.lib(build_if_missing=True)
+
+
+def test_exports_every_header_symbol(L):
+    names = _lib.header_symbols()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_strings(L):
+    assert L.fa_version() >= 100
+    assert L.fa_status_string(_lib.FA_ERR_TIMEOUT) == b"FA_ERR_TIMEOUT"
+    assert L.fa_status_string(99) == b"FA_ERR_UNKNOWN"
+
+
+def test_split_heuristic_page_example(L):
+    g = G["split_count"]
+    n = L.fa_num_splits_heuristic(g["batch"], g["kv_heads"], g["context"], g["num_sms"])
+    assert n == g["splits"]
+    assert g["context"] // n == g["keys_per_split"]
+    assert n * g["kv_heads"] == g["split_blocks"]
+    assert abs(g["split_blocks"] / g["num_sms"] - g["waves"]) < g["tol"]
+    assert abs(g["unsplit_blocks"] / g["num_sms"] - g["unsplit_sm_fraction"]) < g["tol"]
+    # no split once batch x KV heads fills the GPU ("not worth it at high batch")
+    assert L.fa_num_splits_heuristic(64, 8, 8192, 132) == 1
+    assert L.fa_num_splits_heuristic(16, 8, 8192, 132) == 1
+    # GB300: 152 SMs
+    assert L.fa_num_splits_heuristic(1, 8, 131072, 152) == 19
+    # never fewer than 256 keys per split
+    assert L.fa_num_splits_heuristic(1, 1, 1000, 152) == 4
+    assert L.fa_num_splits_heuristic(0, 8, 100, 152) == 1
+
+
+def test_workspace_bytes(L):
+    assert L.fa_decode_workspace_bytes(1, 32, 1, 128, 1) == 0
+    n, rows, d = 16, 32, 128
+    ob = ((n * rows * d * 4 + 255) // 256) * 256
+    assert L.fa_decode_workspace_bytes(1, 32, 1, 128, 16) == ob + n * rows * 4
+
+
+def _fwd(L, *, q=P, k=P, v=P, o=P, lse=None, B=1, Hq=2, Hkv=2, T=8, S=8, d=128, scale=0.125, causal=0):
+    return L.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, T, S, d, scale, causal, None)
+
+
+def test_fwd_rejects_bad_arguments(L):
+    assert _fwd(L, q=None) == _lib.FA_ERR_INVALID_ARG
+    assert _fwd(L, k=MIS) == _lib.FA_ERR_INVALID_ARG
+    assert _fwd(L, Hq=3, Hkv=2) == _lib.FA_ERR_INVALID_ARG
+    assert _fwd(L, T=0) == _lib.FA_ERR_INVALID_ARG
+    assert _fwd(L, S=0) == _lib.FA_ERR_INVALID_ARG
+    assert _fwd(L, scale=0.0) == _lib.FA_ERR_INVALID_ARG
+    assert _fwd(L, scale=float("nan")) == _lib.FA_ERR_INVALID_ARG
+    assert _fwd(L, d=96) == _lib.FA_ERR_UNSUPPORTED
+    assert _fwd(L, Hq=6, Hkv=2) == _lib.FA_ERR_UNSUPPORTED  # group of 3
+    assert _fwd(L, Hq=32, Hkv=1) == _lib.FA_ERR_UNSUPPORTED  # group of 32
+    assert L.fa_fwd_f32(P, P, P, P, None, 1, 1, 1, 4, 4, 200, 0.1, 0, None) == _lib.FA_ERR_UNSUPPORTED
+
+
+def test_decode_rejects_bad_arguments(L):
+    # group 8 x T 3 = 24 stacked rows > 16
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 1, 3, 100, 128, 0.1, 1, 1, None, 0, None) == _lib.FA_ERR_UNSUPPORTED
+    # a split count above one needs a large enough, 256-byte aligned workspace
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 2, 1, 100, 128, 0.1, 1, 4, None, 0, None) == _lib.FA_ERR_INVALID_ARG
+    need = L.fa_decode_workspace_bytes(1, 8, 1, 128, 4)
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 2, 1, 100, 128, 0.1, 1, 4, P, need - 1, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 2, 1, 100, 128, 0.1, 1, 4, ctypes.c_void_p(272), need, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 2, 1, 100, 128, 0.1, 1, -1, None, 0, None) == _lib.FA_ERR_INVALID_ARG
+    # paged: only 16-token pages
+    args = [P, P, P, P, P, P, None, 2, 8, 2, 1, 4, 32, 8, 128, 0.1, 1, 1, None, 0, None]
+    assert L.fa_decode_paged(*args) == _lib.FA_ERR_UNSUPPORTED
+    args[12] = 16
+    args[3] = None  # no block table
+    assert L.fa_decode_paged(*args) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_lse_merge(P, P, P, None, 0, 4, 128, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_lse_merge(P, P, P, None, 2, 4, 512, None) == _lib.FA_ERR_UNSUPPORTED

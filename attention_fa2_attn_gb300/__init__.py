@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     FAError,
     fa_decode_paged,
     fa_decode_splitkv,
+    fa_decode_splitkv_static,
     fa_decode_workspace_bytes,
     fa_fwd,
     fa_fwd_f32,

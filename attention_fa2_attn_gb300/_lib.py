@@ -38,6 +38,7 @@ SIGNATURES = {
     "fa_num_splits_heuristic": (_I, [_I, _I, _I, _I]),
     "fa_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "fa_decode_splitkv_static": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "fa_lse_merge": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "fa_decode_paged": (
         _I,

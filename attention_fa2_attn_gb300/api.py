@@ -107,6 +107,24 @@ def fa_decode_splitkv(q, k, v, causal: bool = True, num_splits: int = 0, scale: 
     return o, lse
 
 
+def fa_decode_splitkv_static(q, k, v, causal: bool = True, num_splits: int = 0, scale: float | None = None,
+                             out=None, lse=None):
+    """Split-KV decode with the partials in the library's fixed 4 MiB device array
+    (no workspace, no allocation inside the call); see include/fa_gb300.h."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Hq, T, d = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_splitkv_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
+                                        int(causal), int(num_splits), _stream(q))
+    check(st, "fa_decode_splitkv_static")
+    return o, lse
+
+
 def fa_lse_merge(o_part, lse_part):
     """Merge o_part [n][rows][d] fp32 and lse_part [n][rows] fp32 -> (o [rows][d] bf16, lse [rows] fp32)."""
     _need(o_part, "o_part", torch.float32, 3)
@@ -170,6 +188,7 @@ __all__ = [
     "fa_num_splits_heuristic",
     "fa_decode_workspace_bytes",
     "fa_decode_splitkv",
+    "fa_decode_splitkv_static",
     "fa_lse_merge",
     "fa_decode_paged",
     "fa_get_last_device_error",

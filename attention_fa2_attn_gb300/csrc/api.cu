@@ -98,6 +98,12 @@ __global__ void selftest_wait_kernel(unsigned* err, unsigned long long timeout_n
   if (threadIdx.x == 0 && !mbar_wait(&bar, 0, timeout_ns)) record_error(err, FA_ERR_TIMEOUT, SITE_SELFTEST);
 }
 
+// Accessors for other translation units of the library.
+unsigned* device_error_word() { return error_word(); }
+unsigned long long wait_timeout_ns() { return g_timeout_ns; }
+int device_sm_count() { return sm_count(); }
+int record_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+
 }  // namespace fa
 
 using namespace fa;

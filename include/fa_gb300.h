@@ -131,6 +131,28 @@ FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, 
                             int num_splits, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * fa_decode_splitkv_static -- fa_decode_splitkv without a workspace argument.
+ * The pages have no counterpart: this serves callers that cannot allocate
+ * device memory for the split partials (work recorded into a CUDA graph
+ * while it is being captured, engines whose device memory is carved up once
+ * by their host, latency-critical paths that must not risk an allocation).
+ * The partials go to a fixed 4 MiB array inside the library's device image
+ * (every device that loads the library holds one until the process exits);
+ * the call allocates nothing.
+ *   Arguments and results as fa_decode_splitkv.
+ *   Returns FA_ERR_UNSUPPORTED when the partials would need more than 4 MiB,
+ *   i.e. fa_decode_workspace_bytes(B, Hq, T, d, splits) > 4194304.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls on a device share the array and it keeps the last call's
+ *   contents (every call rewrites what it reads). Calls that overlap on the
+ *   GPU -- other streams, other host threads -- race on it: serialise them.
+ */
+FA_API fa_status fa_decode_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                                          int B, int Hq, int Hkv, int T, int S, int d, float scale, int causal,
+                                          int num_splits, void* stream);
+
+/*
  * fa_lse_merge -- merge normalised partial results of `num_splits` key ranges.
  * ("Attention kernel chains", "The log-sum-exp merge": lse = ln sum_s e^{lse_s},
  *  O = sum_s e^{lse_s - lse} O_s.)

@@ -10,24 +10,25 @@
 // pass saves").
 //
 // How (GB300-specific):
-//   * one CTA per (batch, KV head, tile of BM = 128 query rows). With GQA the
-//     g query heads of a group are stacked as rows of one tile (128/g
-//     positions x g heads), so every K/V tile is loaded once per group ("GQA
-//     loads KV once per group"). A 4-D TMA box {64, 128/g, g, 1} over Q
-//     [B][Hq][T][d] builds the stacked tile directly.
-//   * warp 4 (one elected thread): TMA producer. Q once, then K_j and V_j
-//     into a 2-stage ring of 128-byte-swizzled shared-memory tiles; separate
-//     full/empty mbarriers for K and V so K can be refilled as soon as
-//     S_j = Q K_j^T has consumed it.
-//   * warp 5: allocates 512 TMEM columns; one thread issues tcgen05.mma.
-//     S_j (fp32, 128 columns) goes to one of two TMEM buffers so S_{j+1} is
-//     computed while the softmax works on S_j; O (fp32, d columns) stays in
-//     TMEM for the whole row of tiles.
-//   * warps 0-3 (128 threads, thread r = row r = TMEM lane r): softmax.
-//     tcgen05.ld of S_j, row max, p = 2^(s*c - m) with c = scale*log2(e)
-//     folded into one FFMA, P packed to bf16 and written to a swizzled smem
-//     tile (the A operand of O += P V_j). O is rescaled in TMEM only when
-//     the max of some row of the warp rose.
+//   * one CTA per (batch, KV head, pair of BM = 128-row query tiles). With GQA
+//     the g query heads of a group are stacked as rows of a tile (128/g
+//     positions x g heads), so every K/V tile is loaded once per group and
+//     serves 256 rows ("GQA loads KV once per group"). A 4-D TMA box
+//     {64, 128/g, g, 1} over Q [B][Hq][T][d] builds a stacked tile directly.
+//   * warp 8 (one elected thread): TMA producer. Both Q tiles once, then K_j
+//     and V_j into a 2-stage ring of 128-byte-swizzled shared-memory tiles,
+//     with separate full/empty mbarriers for K and V.
+//   * warp 9: allocates all 512 TMEM columns -- per query tile t a 128-column
+//     S/P region and a d-column O region -- and one thread issues the
+//     tcgen05.mma chain. The two query tiles ping-pong on the tensor core:
+//     while one tile's softmax runs, the MMAs of the other tile proceed.
+//     S_t = Q_t K_j^T reads both operands from smem; O_t += P_t V_j reads P_t
+//     from TMEM (where the softmax left it) and V_j from smem (MN-major).
+//   * warps 0-3 / 4-7: the softmax of tile 0 / 1, thread r = row r = TMEM
+//     lane r. tcgen05.ld of S, row max, p = 2^(s*c - m) with c =
+//     scale*log2(e) folded into one packed FFMA, P packed to bf16 and written
+//     back over S with tcgen05.st. O is rescaled in TMEM only when the max of
+//     some row of the warp rose.
 //   * causal: tiles entirely above the diagonal are never loaded or issued;
 //     the mask is evaluated only on tiles that cross it (or the ragged end).
 //     CTAs are ordered heaviest first.
@@ -40,25 +41,26 @@ namespace fa {
 
 template <int D>
 struct PfCfg {
-  static constexpr int BM = 128;           // query rows per tile (TMEM lanes)
-  static constexpr int BN = 128;           // keys per K/V tile
-  static constexpr int KCH = D / 64;       // 64-element (128-byte) chunks along d
-  static constexpr int STAGES = 2;         // K/V ring depth
+  static constexpr int BM = 128;                 // query rows per tile (TMEM lanes)
+  static constexpr int QT = 2;                   // query tiles per CTA
+  static constexpr int BN = 128;                 // keys per K/V tile
+  static constexpr int KCH = D / 64;             // 64-element (128-byte) chunks along d
+  static constexpr int STAGES = 2;               // K/V ring depth
   static constexpr int CHUNK_BYTES = 128 * 128;  // one 128-row x 128-byte swizzled chunk
-  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int Q_BYTES = BM * D * 2;     // one query tile
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int P_BYTES = BM * BN * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + QT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + slack to align the base to 1024
   static constexpr int TMEM_COLS = 512;
-  static constexpr int S_COL1 = 128;  // S buffer b lives at column b * S_COL1
-  static constexpr int O_COL = 256;
-  static constexpr int THREADS = 192;
+  static constexpr int TILE_COLS = 256;   // TMEM columns per query tile: S/P then O
+  static constexpr int O_OFF = 128;       // O region inside a tile's columns
+  static constexpr int THREADS = 320;     // 2 softmax warpgroups + producer warp + MMA warp
+  static constexpr int PRODUCER_WARP = 8;
+  static constexpr int MMA_WARP = 9;
 };
 
 struct PfParams {
@@ -68,6 +70,7 @@ struct PfParams {
   int g;              // query heads per KV head
   int rows_per_head;  // 128 / g query positions per tile
   int n_qtiles;       // ceil(T / rows_per_head)
+  int n_pairs;        // ceil(n_qtiles / 2)
   int causal;
   float c;            // scale * log2(e)
   unsigned* err;
@@ -77,14 +80,16 @@ struct PfParams {
 struct PfBars {
   uint64_t q_full;
   uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, drain;
+  uint64_t s_full[2];   // per query tile: S_t(j) computed
+  uint64_t p_full[2];   // per query tile: P_t(j) in TMEM (and O_t rescaled)
+  uint64_t pv_done[2];  // per query tile: O_t += P_t(j) V_j finished
+  uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PfParams p) {
   using C = PfCfg<D>;
@@ -93,32 +98,36 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sP = smem + C::OFF_P;
   PfBars* bars = reinterpret_cast<PfBars*>(smem + C::OFF_BAR);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (b, kv head, query tile); causal runs heaviest tiles first
+  // ---- work item: (b, kv head, pair of query tiles); causal runs heaviest pairs first
   const int bh_count = p.B * p.Hkv;
-  int qt, bh;
+  int qp, bh;
   if (p.causal) {
-    qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / bh_count;
+    qp = p.n_pairs - 1 - static_cast<int>(blockIdx.x) / bh_count;
     bh = static_cast<int>(blockIdx.x) % bh_count;
   } else {
-    bh = static_cast<int>(blockIdx.x) / p.n_qtiles;
-    qt = static_cast<int>(blockIdx.x) % p.n_qtiles;
+    bh = static_cast<int>(blockIdx.x) / p.n_pairs;
+    qp = static_cast<int>(blockIdx.x) % p.n_pairs;
   }
   const int b = bh / p.Hkv;
   const int kvh = bh % p.Hkv;
-  const int p0 = qt * p.rows_per_head;  // first query position of the tile
-  const int shift = p.S - p.T;           // bottom-right alignment: row i sees keys j <= i + shift
-  int kv_end = p.S;
-  if (p.causal) {
-    const int last_pos = min(p0 + p.rows_per_head, p.T) - 1;
-    kv_end = min(p.S, last_pos + shift + 1);
+  const int shift = p.S - p.T;  // bottom-right alignment: row i sees keys j <= i + shift
+  int p0[2], njt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    p0[t] = (2 * qp + t) * p.rows_per_head;  // first query position of tile t
+    int kv_end = 0;
+    if (p0[t] < p.T) {
+      kv_end = p.S;
+      if (p.causal) kv_end = min(p.S, min(p0[t] + p.rows_per_head, p.T) - 1 + shift + 1);
+    }
+    njt[t] = kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
   }
-  const int nj = kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
+  const int nj = max(njt[0], njt[1]);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -128,15 +137,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 128);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->pv_done[s], 1);
     }
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+  if (warp == C::MMA_WARP) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
@@ -148,15 +156,16 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 1;
   };
 
-  if (warp == 4) {
+  if (warp == C::PRODUCER_WARP) {
     // ======================= TMA producer =======================
     if (lane == 0 && nj > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(sQ + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, p0, kvh * p.g, b);
+      mbar_arrive_expect_tx(&bars->q_full, C::QT * C::Q_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, p0[t], kvh * p.g, b);
       int issued = 0;
       for (int j = 0; j < nj; ++j) {
         const int s = j % C::STAGES;
@@ -170,8 +179,7 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, j * C::BN, bh);
         if (j >= C::STAGES && !mbar_wait(&bars->v_empty[s], (u - 1) & 1, tmo, abort_flag)) {
           fail(SITE_PF_PRODUCER);
-          // K_j was issued: let its copy land before the CTA's smem goes away
-          mbar_wait(&bars->k_full[s], u & 1, tmo);
+          mbar_wait(&bars->k_full[s], u & 1, tmo);  // K_j was issued: let it land
           break;
         }
         mbar_arrive_expect_tx(&bars->v_full[s], C::KV_BYTES);
@@ -180,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
         issued = j + 1;
       }
       if (*abort_flag) {
-        // drain: copies still in flight must complete before the CTA exits
+        // copies still in flight must complete before the CTA exits
         mbar_wait(&bars->q_full, 0, tmo);
         for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
           mbar_wait(&bars->k_full[j % C::STAGES], (j / C::STAGES) & 1, tmo);
@@ -188,72 +196,94 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == C::MMA_WARP) {
     // ======================= MMA issuer =======================
     if (lane == 0 && nj > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, C::BN, 0, 0);  // A = Q (K-major), B = K (K-major)
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);      // A = P (K-major), B = V (MN-major)
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV), sPa = smem_u32(sP);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);      // A = P (TMEM), B = V (MN-major)
+      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
       bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j % C::STAGES;
-        if (!mbar_wait(&bars->k_full[s], (j / C::STAGES) & 1, tmo, abort_flag)) return false;
-        if (j >= 2 && !mbar_wait(&bars->s_free[j & 1], ((j >> 1) & 1) ^ 1, tmo, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t kbase = sKa + s * C::KV_BYTES;
+      tc_fence_after();
+      // S_t(j) = Q_t K_j^T into tile t's S/P columns
+      auto qk = [&](int t, int j) {
+        const uint32_t kbase = sKa + (j % C::STAGES) * C::KV_BYTES;
+        const uint32_t qbase = sQa + t * C::Q_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // 16 elements of d per MMA: chunk kk/4, 32-byte step inside the 128-byte swizzle row
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          tc_mma_ss(tmem + (j & 1) * C::S_COL1, smem_desc_sw128(sQa + off, 16, 1024),
+          tc_mma_ss(tmem + t * C::TILE_COLS, smem_desc_sw128(qbase + off, 16, 1024),
                     smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&bars->k_empty[s]);
-        tc_commit(&bars->s_full[j & 1]);
-        return true;
+        tc_commit(&bars->s_full[t]);
       };
-      if (ok) ok = issue_qk(0);
-      for (int j = 0; ok && j < nj; ++j) {
-        if (j + 1 < nj && !issue_qk(j + 1)) {
-          ok = false;
-          break;
-        }
-        const int s = j % C::STAGES;
-        if (!mbar_wait(&bars->p_full, j & 1, tmo, abort_flag) ||
-            !mbar_wait(&bars->v_full[s], (j / C::STAGES) & 1, tmo, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t vbase = sVa + s * C::KV_BYTES;
+      // O_t += P_t(j) V_j: P from TMEM (8 columns = 16 keys per MMA), V MN-major from smem
+      auto pv = [&](int t, int j) {
+        const uint32_t vbase = sVa + (j % C::STAGES) * C::KV_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          // A = P: 16 keys per MMA (chunk kk/4 of the swizzled P tile);
-          // B = V, MN-major: 16 keys = two 8-row groups of 1024 bytes; LBO steps over d chunks
-          const uint32_t poff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          tc_mma_ss(tmem + C::O_COL, smem_desc_sw128(sPa + poff, 16, 1024),
-                    smem_desc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          tc_mma_ts(tmem + t * C::TILE_COLS + C::O_OFF, tmem + t * C::TILE_COLS + kk * 8,
+                    smem_desc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars->pv_done[t]);
+      };
+      if (ok) {
+        ok = mbar_wait(&bars->k_full[0], 0, tmo, abort_flag);
+        tc_fence_after();
+        if (ok) {
+          for (int t = 0; t < 2; ++t)
+            if (njt[t] > 0) qk(t, 0);
+          tc_commit(&bars->k_empty[0]);
         }
+      }
+      for (int j = 0; ok && j < nj; ++j) {
+        const int s = j % C::STAGES;
+        bool k_next_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= njt[t]) continue;
+          if (!mbar_wait(&bars->p_full[t], j & 1, tmo, abort_flag) ||
+              !mbar_wait(&bars->v_full[s], (j / C::STAGES) & 1, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          pv(t, j);
+          // the next S of this tile overwrites the columns P_t(j) is read from; MMAs
+          // issued by one thread execute in order, so it is queued right behind
+          if (j + 1 < njt[t]) {
+            if (!k_next_ready) {
+              if (!mbar_wait(&bars->k_full[(j + 1) % C::STAGES], ((j + 1) / C::STAGES) & 1, tmo, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_next_ready = true;
+            }
+            qk(t, j + 1);
+          }
+        }
+        if (!ok) break;
         tc_commit(&bars->v_empty[s]);
-        tc_commit(&bars->o_done);
+        if (k_next_ready) tc_commit(&bars->k_empty[(j + 1) % C::STAGES]);
       }
-      if (!ok) {
-        fail(SITE_PF_MMA);
-        // every MMA issued so far must finish before TMEM is released
-        tc_commit(&bars->drain);
-        mbar_wait(&bars->drain, 0, tmo);
-      }
+      if (!ok) fail(SITE_PF_MMA);
+      // every MMA issued must finish before TMEM is released
+      tc_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, tmo);
     }
   } else {
-    // ======================= softmax: warps 0-3, one row per thread =======================
-    const int r = threadIdx.x;  // row of the tile == TMEM lane
+    // ======================= softmax: warps 0-3 (tile 0), 4-7 (tile 1) =======================
+    const int t = warp >> 2;
+    const int r = threadIdx.x & 127;  // row of the tile == TMEM lane
     const int h_local = r / p.rows_per_head;
-    const int pos = p0 + (r % p.rows_per_head);
+    const int pos = p0[t] + (r % p.rows_per_head);
     const bool row_valid = pos < p.T;
     const int vis_last = pos + shift;  // causal: last visible key of this row
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * C::TILE_COLS;
+    const uint32_t tO = tS + C::O_OFF;
+    const int my_nj = njt[t];
     const float c = p.c;
+    const float2 c2 = make_float2(c, c);
     float m = -INFINITY;  // running max, in units of log2 (scores times c)
     float l = 0.f;        // running sum of 2^(s*c - m)
     bool ok = true;
@@ -263,90 +293,101 @@ __global__ void __launch_bounds__(192, 1)
       const bool w = mbar_wait(bar, parity, tmo, abort_flag);
       return __all_sync(0xffffffffu, w);
     };
-    uint8_t* prow = sP + r * 128;
-    const int rsw = r & 7;
 
-    for (int j = 0; j < nj; ++j) {
-      const int sb = j & 1;
-      if (!wwait(&bars->s_full[sb], (j >> 1) & 1)) {
+    for (int j = 0; j < my_nj; ++j) {
+      if (!wwait(&bars->s_full[t], j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // S row: four 32-column loads in flight, one wait
+      uint32_t raw[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, raw[cc]);
+      tmem_ld_wait();
       float s[128];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t raw[32];
-        tmem_ld32(tmem + lane_base + sb * C::S_COL1 + cc * 32, raw);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(raw[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[sb]);
+      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
 
       const int key0 = j * C::BN;
-      const bool need_mask = (key0 + C::BN > p.S) || (p.causal && key0 + C::BN - 1 > p0 + shift);
+      const bool need_mask = (key0 + C::BN > p.S) || (p.causal && key0 + C::BN - 1 > p0[t] + shift);
       if (need_mask) {
-        const int lim = p.causal ? min(p.S - 1, vis_last) : p.S - 1;
+        const int lim = (p.causal ? min(p.S - 1, vis_last) : p.S - 1) - key0;
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (key0 + i > lim) s[i] = -INFINITY;
+          if (i > lim) s[i] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: eight independent three-input chains, then a short tree
+      float mx8[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      for (int k = 0; k < 8; ++k) {
+        float a = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
+#pragma unroll
+        for (int i = 3; i < 15; i += 2) a = fmax3(a, s[16 * k + i], s[16 * k + i + 1]);
+        mx8[k] = fmaxf(a, s[16 * k + 15]);
+      }
+      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       const float m_new = fmaxf(m, mx * c);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_use);  // 0 while nothing was seen (m = -inf)
-      float rs = 0.f;
-      uint32_t pk[64];
+      // p = 2^(s*c - m): packed FFMA, MUFU ex2, bf16 pairs stored over S, 32 columns at a time
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float e0 = ex2_approx(fmaf(s[2 * i], c, -m_use));
-        const float e1 = ex2_approx(fmaf(s[2 * i + 1], c, -m_use));
-        rs += e0 + e1;
-        pk[i] = pack_bf16x2(e0, e1);
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = cc * 32 + 2 * i;
+          const float2 x = ffma2(make_float2(s[e], s[e + 1]), c2, nm2);
+          const float2 ev = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[i & 3] = fadd2(acc[i & 3], ev);
+          pk[i] = pack_bf16x2(ev.x, ev.y);
+        }
+        tmem_st16(tS + cc * 16, pk);  // keys 32cc .. 32cc+31 -> columns 16cc .. 16cc+15
       }
-      l = l * alpha + rs;
+      const float2 a01 = fadd2(acc[0], acc[1]);
+      const float2 a23 = fadd2(acc[2], acc[3]);
+      const float2 at = fadd2(a01, a23);
+      l = fmaf(l, alpha, at.x + at.y);
       m = m_new;
 
-      if (j > 0) {
-        // PV_{j-1} must be done: it reads the P tile and accumulates into O
-        if (!wwait(&bars->o_done, (j - 1) & 1)) {
+      // O is rescaled only when the max of some row of this warp rose; that
+      // needs PV_t(j-1) finished (it accumulates into O)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!wwait(&bars->pv_done[t], (j - 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            const uint32_t addr = tmem + lane_base + C::O_COL + cc * 32;
-            tmem_ld32(addr, o);
-            tmem_ld_wait();
+        for (int cc = 0; cc < D / 32; cc += 2) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO + cc * 32, o0);
+          tmem_ld32(tO + cc * 32 + 32, o1);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(addr, o);
+          for (int i = 0; i < 32; i += 2) {
+            float2 v0 = fmul2(make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), al2);
+            float2 v1 = fmul2(make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), al2);
+            o0[i] = __float_as_uint(v0.x);
+            o0[i + 1] = __float_as_uint(v0.y);
+            o1[i] = __float_as_uint(v1.x);
+            o1[i + 1] = __float_as_uint(v1.y);
           }
-          tmem_st_wait();
+          tmem_st32(tO + cc * 32, o0);
+          tmem_st32(tO + cc * 32 + 32, o1);
         }
       }
-      // P row -> swizzled K-major tile: 16-byte piece q of chunk (keys 64*ch ..) at (q ^ (r % 8))
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int ch = q >> 3, qi = q & 7;
-        uint4 v = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        *reinterpret_cast<uint4*>(prow + ch * C::CHUNK_BYTES + ((qi ^ rsw) << 4)) = v;
-      }
-      fence_async_smem();
+      tmem_st_wait();  // P (and O) stores complete before the MMA may read them
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(&bars->p_full[t]);
     }
 
     // ---- epilogue: O / l -> bf16, lse = ln2 * (m + log2 l)
-    if (ok && nj > 0) {
-      if (!wwait(&bars->o_done, (nj - 1) & 1)) ok = false;
+    if (ok && my_nj > 0) {
+      if (!wwait(&bars->pv_done[t], (my_nj - 1) & 1)) ok = false;
       tc_fence_after();
     }
     if (!ok) fail(SITE_PF_SOFTMAX);
@@ -358,8 +399,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        if (nj > 0) {
-          tmem_ld32(tmem + lane_base + C::O_COL + cc * 32, o);
+        if (my_nj > 0) {
+          tmem_ld32(tO + cc * 32, o);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -383,7 +424,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -436,11 +477,12 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, floa
   p.g = g;
   p.rows_per_head = rows_per_head;
   p.n_qtiles = (T + rows_per_head - 1) / rows_per_head;
+  p.n_pairs = (p.n_qtiles + 1) / 2;
   p.causal = causal;
   p.c = scale * kLog2e;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  const long long grid = static_cast<long long>(p.n_qtiles) * B * Hkv;
+  const long long grid = static_cast<long long>(p.n_pairs) * B * Hkv;
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (d == 128) {
     auto kfn = prefill_tc_kernel<128>;

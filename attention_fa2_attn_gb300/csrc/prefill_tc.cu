@@ -58,9 +58,15 @@ struct PfCfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int TILE_COLS = 256;   // TMEM columns per query tile: S/P then O
   static constexpr int O_OFF = 128;       // O region inside a tile's columns
-  static constexpr int THREADS = 320;     // 2 softmax warpgroups + producer warp + MMA warp
+  // warpgroups 0 and 1: softmax of tile 0 and 1; warpgroup 2: producer warp,
+  // MMA warp and two idle warps. Launched at 168 registers a thread; warpgroup
+  // 2 gives back down to 120 and the softmax warpgroups take up to 192:
+  // 256 * 192 + 128 * 120 = 64512 = 384 * 168.
+  static constexpr int THREADS = 384;
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
+  static constexpr int SOFTMAX_REGS = 192;
+  static constexpr int AUX_REGS = 120;
 };
 
 struct PfParams {
@@ -89,7 +95,7 @@ struct PfBars {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PfParams p) {
   using C = PfCfg<D>;
@@ -116,18 +122,21 @@ __global__ void __launch_bounds__(320, 1)
   const int b = bh / p.Hkv;
   const int kvh = bh % p.Hkv;
   const int shift = p.S - p.T;  // bottom-right alignment: row i sees keys j <= i + shift
-  int p0[2], njt[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    p0[t] = (2 * qp + t) * p.rows_per_head;  // first query position of tile t
+  // first query position and number of key tiles of query tile t (scalars, not
+  // arrays: a runtime-indexed array would live in local memory)
+  auto tile_nj = [&](int first_pos) -> int {
     int kv_end = 0;
-    if (p0[t] < p.T) {
+    if (first_pos < p.T) {
       kv_end = p.S;
-      if (p.causal) kv_end = min(p.S, min(p0[t] + p.rows_per_head, p.T) - 1 + shift + 1);
+      if (p.causal) kv_end = min(p.S, min(first_pos + p.rows_per_head, p.T) - 1 + shift + 1);
     }
-    njt[t] = kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
-  }
-  const int nj = max(njt[0], njt[1]);
+    return kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
+  };
+  const int p0_0 = (2 * qp) * p.rows_per_head;
+  const int p0_1 = p0_0 + p.rows_per_head;
+  const int nj_0 = tile_nj(p0_0);
+  const int nj_1 = tile_nj(p0_1);
+  const int nj = max(nj_0, nj_1);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -156,6 +165,10 @@ __global__ void __launch_bounds__(320, 1)
     *abort_flag = 1;
   };
 
+  if (warp >= 8) {
+    // setmaxnreg is issued at the head of each role's branch so that the
+    // register budget it sets governs all of that role's code
+    warpgroup_reg_dealloc<C::AUX_REGS>();
   if (warp == C::PRODUCER_WARP) {
     // ======================= TMA producer =======================
     if (lane == 0 && nj > 0) {
@@ -165,7 +178,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_expect_tx(&bars->q_full, C::QT * C::Q_BYTES);
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, p0[t], kvh * p.g, b);
+          tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, t ? p0_1 : p0_0,
+                      kvh * p.g, b);
       int issued = 0;
       for (int j = 0; j < nj; ++j) {
         const int s = j % C::STAGES;
@@ -201,37 +215,44 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0 && nj > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, C::BN, 0, 0);  // A = Q (K-major), B = K (K-major)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);      // A = P (TMEM), B = V (MN-major)
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      // descriptors of the operand bases; an MMA adds its (compile-time) byte offset >> 4
+      // to the start-address field, which never carries out of its 14 bits (smem < 256 KB)
+      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = smem_desc_sw128(smem_u32(sV), C::CHUNK_BYTES, 1024);
       bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
       tc_fence_after();
       // S_t(j) = Q_t K_j^T into tile t's S/P columns
-      auto qk = [&](int t, int j) {
-        const uint32_t kbase = sKa + (j % C::STAGES) * C::KV_BYTES;
-        const uint32_t qbase = sQa + t * C::Q_BYTES;
+      auto qk = [=](int t, int j) {
+        const uint64_t a0 = dQ + static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
+        const uint64_t b0 = dK + static_cast<uint64_t>(((j % C::STAGES) * C::KV_BYTES) >> 4);
+        const uint32_t dS = tmem + t * C::TILE_COLS;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // 16 elements of d per MMA: chunk kk/4, 32-byte step inside the 128-byte swizzle row
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          tc_mma_ss(tmem + t * C::TILE_COLS, smem_desc_sw128(qbase + off, 16, 1024),
-                    smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(dS, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&bars->s_full[t]);
       };
       // O_t += P_t(j) V_j: P from TMEM (8 columns = 16 keys per MMA), V MN-major from smem
-      auto pv = [&](int t, int j) {
-        const uint32_t vbase = sVa + (j % C::STAGES) * C::KV_BYTES;
+      auto pv = [=](int t, int j) {
+        const uint64_t b0 = dV + static_cast<uint64_t>(((j % C::STAGES) * C::KV_BYTES) >> 4);
+        const uint32_t dO = tmem + t * C::TILE_COLS + C::O_OFF;
+        const uint32_t aP = tmem + t * C::TILE_COLS;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_ts(tmem + t * C::TILE_COLS + C::O_OFF, tmem + t * C::TILE_COLS + kk * 8,
-                    smem_desc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&bars->pv_done[t]);
+          tc_mma_ts(dO, aP + kk * 8, b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
       };
       if (ok) {
         ok = mbar_wait(&bars->k_full[0], 0, tmo, abort_flag);
         tc_fence_after();
         if (ok) {
           for (int t = 0; t < 2; ++t)
-            if (njt[t] > 0) qk(t, 0);
+            if ((t ? nj_1 : nj_0) > 0) {
+              qk(t, 0);
+              tc_commit(&bars->s_full[t]);
+            }
           tc_commit(&bars->k_empty[0]);
         }
       }
@@ -239,7 +260,8 @@ __global__ void __launch_bounds__(320, 1)
         const int s = j % C::STAGES;
         bool k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= njt[t]) continue;
+          const int njt = t ? nj_1 : nj_0;
+          if (j >= njt) continue;
           if (!mbar_wait(&bars->p_full[t], j & 1, tmo, abort_flag) ||
               !mbar_wait(&bars->v_full[s], (j / C::STAGES) & 1, tmo, abort_flag)) {
             ok = false;
@@ -247,9 +269,10 @@ __global__ void __launch_bounds__(320, 1)
           }
           tc_fence_after();
           pv(t, j);
+          tc_commit(&bars->pv_done[t]);
           // the next S of this tile overwrites the columns P_t(j) is read from; MMAs
           // issued by one thread execute in order, so it is queued right behind
-          if (j + 1 < njt[t]) {
+          if (j + 1 < njt) {
             if (!k_next_ready) {
               if (!mbar_wait(&bars->k_full[(j + 1) % C::STAGES], ((j + 1) / C::STAGES) & 1, tmo, abort_flag)) {
                 ok = false;
@@ -259,6 +282,7 @@ __global__ void __launch_bounds__(320, 1)
               k_next_ready = true;
             }
             qk(t, j + 1);
+            tc_commit(&bars->s_full[t]);
           }
         }
         if (!ok) break;
@@ -270,18 +294,21 @@ __global__ void __launch_bounds__(320, 1)
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, tmo);
     }
+  }
   } else {
     // ======================= softmax: warps 0-3 (tile 0), 4-7 (tile 1) =======================
+    warpgroup_reg_alloc<C::SOFTMAX_REGS>();
     const int t = warp >> 2;
     const int r = threadIdx.x & 127;  // row of the tile == TMEM lane
     const int h_local = r / p.rows_per_head;
-    const int pos = p0[t] + (r % p.rows_per_head);
+    const int my_p0 = t ? p0_1 : p0_0;
+    const int pos = my_p0 + (r % p.rows_per_head);
     const bool row_valid = pos < p.T;
     const int vis_last = pos + shift;  // causal: last visible key of this row
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * C::TILE_COLS;
     const uint32_t tO = tS + C::O_OFF;
-    const int my_nj = njt[t];
+    const int my_nj = t ? nj_1 : nj_0;
     const float c = p.c;
     const float2 c2 = make_float2(c, c);
     float m = -INFINITY;  // running max, in units of log2 (scores times c)
@@ -310,7 +337,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
 
       const int key0 = j * C::BN;
-      const bool need_mask = (key0 + C::BN > p.S) || (p.causal && key0 + C::BN - 1 > p0[t] + shift);
+      const bool need_mask = (key0 + C::BN > p.S) || (p.causal && key0 + C::BN - 1 > my_p0 + shift);
       if (need_mask) {
         const int lim = (p.causal ? min(p.S - 1, vis_last) : p.S - 1) - key0;
 #pragma unroll

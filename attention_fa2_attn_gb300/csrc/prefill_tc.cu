@@ -311,8 +311,16 @@ __global__ void __launch_bounds__(384, 1)
     const int my_nj = t ? nj_1 : nj_0;
     const float c = p.c;
     const float2 c2 = make_float2(c, c);
-    float m = -INFINITY;  // running max, in units of log2 (scores times c)
-    float l = 0.f;        // running sum of 2^(s*c - m)
+    // m: the row's reference max, in units of log2 (scores times c); l: the running
+    // sum of 2^(s*c - m); O in TMEM holds the matching unnormalised sum of P V.
+    // The reference is raised (and l, O rescaled by 2^(m_old - m_new)) only when
+    // the row max climbs more than kRescaleSlack above it; below that the
+    // exponentials are taken against the slightly stale reference and stay
+    // <= 2^kRescaleSlack. Every term then carries the same constant factor,
+    // which O / l cancels, so the result is the same softmax.
+    constexpr float kRescaleSlack = 8.f;
+    float m = -INFINITY;
+    float l = 0.f;
     bool ok = true;
     // waits are warp-collective: the warp leaves together, so the .sync.aligned
     // tcgen05 loads and the votes below always see all 32 lanes
@@ -354,9 +362,10 @@ __global__ void __launch_bounds__(384, 1)
         mx8[k] = fmaxf(a, s[16 * k + 15]);
       }
       const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-      const float m_new = fmaxf(m, mx * c);
+      const float m_tile = mx * c;
+      const float m_new = (m_tile > m + kRescaleSlack) ? m_tile : m;  // m = -inf: first visible key sets it
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);  // 0 while nothing was seen (m = -inf)
+      const float alpha = ex2_approx(m - m_use);  // 1 if the reference is kept; 0 while nothing was seen
       // p = 2^(s*c - m): packed FFMA, MUFU ex2, bf16 pairs stored over S, 32 columns at a time
       const float2 nm2 = make_float2(-m_use, -m_use);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};

@@ -110,9 +110,11 @@ def test_large_scores_stay_finite():
     o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, True)
     o, l = _fa().fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=scale)
     assert float(np.abs(l_ref[np.isfinite(l_ref)]).max()) > 300
-    # scores this large make P nearly one-hot: bf16 rounding of a dominant
-    # weight near 1 is the only error, so the bf16 tolerances still hold
-    compare(o, l, o_ref, l_ref, what="large scores")
+    # Scores this large make P nearly one-hot, so O is close to single V rows
+    # (|v| up to ~4) and the bf16 rounding of O itself reaches 2^-9 relative;
+    # the max bound adds 2^-8 |O| to the 1e-2 absolute tolerance. Mean and
+    # lse tolerances are the standard ones.
+    compare(o, l, o_ref, l_ref, o_rel=2.0**-8, what="large scores")
 
 
 def _sampled_check(w, n_rows, seed):

@@ -16,8 +16,9 @@
 //
 // How (GB300-specific): decode reads every K/V byte once and does 2*g FLOP
 // per byte, so it is bound by HBM bandwidth. One producer warp streams
-// 64-key K and V tiles with TMA (128-byte swizzle) into a 6-stage shared
-// memory ring -- 192 KB in flight per SM -- and the four consumer warps each
+// 64-key K and V tiles with TMA (128-byte swizzle) into a shared-memory ring
+// (4 stages of 32 KB, one CTA per SM, for contiguous K/V; 3 stages, two CTAs
+// per SM, for paged K/V) -- 128 KB or more in flight per SM -- and the four consumer warps each
 // take 16 keys of every tile. The 16 x 16 score block and the 16 x d output
 // update of a warp are warp-level bf16 MMAs (m16n8k16), so the ALUs stay far
 // from being a second bound; each warp keeps its own running max / sum /
@@ -85,8 +86,11 @@ __device__ __forceinline__ uint32_t sw_off(int row, int d, int chunk_bytes) {
   return ch * chunk_bytes + row * 128 + ((piece ^ (row & 7)) << 4) + ((d & 7) << 1);
 }
 
+// Paged decode runs two CTAs per SM (3-stage ring, 96 KB each): with 16-token
+// pages a sequence is many small boxes, and two independent streams per SM keep
+// more of them in flight. Contiguous split-KV runs one CTA per SM (4 stages).
 template <int D, int STAGES, bool PAGED>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(160, PAGED ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecParams p) {
   using C = DecCfg<D, STAGES>;
@@ -347,6 +351,9 @@ __global__ void __launch_bounds__(160, 1)
       }
     }
 
+    // the LSE merge of the split partials (a dependent launch) may be scheduled now;
+    // it still waits for this grid to finish before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // ---- merge the four warps' (m, l, O) through shared memory
     float lt[2];
 #pragma unroll
@@ -427,6 +434,9 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float* __restrict_
                                                         const float* __restrict__ lse_part,
                                                         __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                                         int n, int rows, int d) {
+  // launched as a programmatic dependent of the split kernel: wait until that grid
+  // has finished and its partials are visible (a no-op for a plain launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
   if (row >= rows) return;
@@ -475,20 +485,41 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();
 
-constexpr int kDecStages = 6;
+template <bool PAGED>
+constexpr int dec_stages() { return PAGED ? 3 : 4; }
+
+// `after_split`: launched right behind the split kernel on the same stream, as a
+// programmatic dependent (its launch overlaps the split kernel's tail).
+static int launch_lse_merge_impl(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows,
+                                 int d, cudaStream_t stream, bool after_split) {
+  const int grid = (rows + 3) / 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_split ? 1 : 0;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+  if (cudaLaunchKernelEx(&cfg, lse_merge_kernel, o_part, lse_part, ob, lse, n, rows, d) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows, int d,
                      cudaStream_t stream) {
-  const int grid = (rows + 3) / 4;
-  lse_merge_kernel<<<grid, 128, 0, stream>>>(o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, n, rows, d);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_lse_merge_impl(o_part, lse_part, o, lse, n, rows, d, stream, false);
 }
 
 template <int D, bool PAGED>
 static int launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int nsplit, int nbh,
                            cudaStream_t stream) {
-  using C = DecCfg<D, kDecStages>;
-  auto kfn = decode_kernel<D, kDecStages, PAGED>;
+  constexpr int ST = dec_stages<PAGED>();
+  using C = DecCfg<D, ST>;
+  auto kfn = decode_kernel<D, ST, PAGED>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
   dim3 grid(nsplit, nbh);
@@ -564,7 +595,8 @@ int launch_decode(const void* q, const void* k, const void* v, const int* block_
     rc = paged ? launch_decode_t<64, true>(tk, tv, p, num_splits, nbh, stream)
                : launch_decode_t<64, false>(tk, tv, p, num_splits, nbh, stream);
   if (rc != FA_OK || num_splits == 1) return rc;
-  return launch_lse_merge(p.o_part, p.lse_part, o, lse, num_splits, static_cast<int>(rows_total), d, stream);
+  return launch_lse_merge_impl(p.o_part, p.lse_part, o, lse, num_splits, static_cast<int>(rows_total), d, stream,
+                               true);
 }
 
 }  // namespace fa

@@ -70,6 +70,9 @@ def load_traffic():
 # clocks sampled during the timed region
 # --------------------------------------------------------------------------- #
 class ClockSampler:
+    """nvidia-smi samples (every 50 ms) stamped on arrival; stop() keeps those inside
+    the marked timed window."""
+
     FIELDS = (
         "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -79,30 +82,53 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.t0 = self.t1 = 0.0
+        self.lines = []
+        self.t0 = self.t1 = None
+        self.reader = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line))
 
     def start(self):
+        import threading
+
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.idx)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except (OSError, ValueError):
             self.proc = None
-        time.sleep(0.3)
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        time.sleep(0.5)  # let nvidia-smi start sampling before the timed region
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        if self.reader is not None:
+            self.reader.join(timeout=5)
         sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        lo = (self.t0 or 0.0) - 0.05
+        hi = (self.t1 or float("inf")) + 0.05
+        for ts, line in self.lines:
+            if not lo <= ts <= hi:
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -115,14 +141,32 @@ class ClockSampler:
             for n, val in zip(names, f[5:9]):
                 if val.lower() == "active":
                     reasons.add(n)
-        busy = [s for s, p in zip(sm, power) if p > 200] or sm
         return {
-            "sm_mhz": statistics.median(busy) if busy else None,
+            "sm_mhz": statistics.median(sm) if sm else None,
             "sm_max_mhz": max(mx) if mx else None,
             "reasons": sorted(reasons),
             "samples": len(sm),
+            "power_w_median": statistics.median(power) if power else None,
             "power_w_max": max(power) if power else None,
+            "window_s": (self.t1 - self.t0) if (self.t0 and self.t1) else None,
         }
+
+
+def combine_ranks(ms_local: float, world: int) -> float:
+    """Maximum over ranks of a per-rank time (the job is as slow as its slowest rank)."""
+    if world <= 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms_local], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def job_throughput(work_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job rate: every rank processes its own replica of the workload (weak scaling)."""
+    return work_per_rank * world / (ms_per_step * 1e-3)
 
 
 # --------------------------------------------------------------------------- #
@@ -275,7 +319,8 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     gbs = byt / (ms * 1e-3) / 1e9
     out[w.name] = {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
                    "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "launches_per_step": 2,
-                   "bytes_per_step": byt, "num_splits": w.num_splits}
+                   "bytes_per_step": byt, "num_splits": w.num_splits,
+                   "traffic": load_traffic().get("decode_kernel_splitkv")}
     del q, k, v, o, lse, ws
 
     # paged decode
@@ -300,7 +345,8 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     gbs = byt / (ms * 1e-3) / 1e9
     out[w.name] = {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
                    "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "launches_per_step": 1,
-                   "bytes_per_step": byt, "num_splits": 1}
+                   "bytes_per_step": byt, "num_splits": 1,
+                   "traffic": load_traffic().get("decode_kernel_paged")}
     del q, kp, vp, table, sl, o, lse
     torch.cuda.empty_cache()
     return out
@@ -345,18 +391,17 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    sampler.mark_start()
     ms = time_steps(torch, step, args.steps, stream)
     torch.cuda.synchronize()
+    sampler.mark_end()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
+    ms = combine_ranks(ms, world)
 
     flops = cm.attention_flops(w.B, w.Hq, w.T, w.S, w.d, w.causal)
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms) / 1e12
     achieved = flops / (ms * 1e-3) / 1e12  # one prefill launch per step
     peak = peaks["bf16_tflops"]
     traffic = load_traffic().get("prefill_tc_kernel")
@@ -383,10 +428,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
     t0 = time.perf_counter()
     ms_e2e_dev = time_steps(torch, e2e_step, k_e2e, stream)
     ms_e2e = max(ms_e2e_dev, (time.perf_counter() - t0) * 1e3 / k_e2e)
-    if world > 1:
-        t = torch.tensor([ms_e2e], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t[0])
+    ms_e2e = combine_ranks(ms_e2e, world)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
     del qh, kh, vh, oh, lh
@@ -434,7 +476,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
                          "frac": achieved / peak, "traffic": traffic, "kernel": "prefill_tc_kernel<128>",
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                          else "fallback 1.9 PFLOP/s bf16 burst"},
-            "e2e": {"value": flops / (ms_e2e * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+            "e2e": {"value": job_throughput(flops, world, ms_e2e) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
             "cpu_baseline": cpu,
             "clocks": clocks,
@@ -453,7 +495,7 @@ def main() -> int:
         return 0
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true")

@@ -81,6 +81,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One lane of the (fully active) warp, the same one in every call: the issuer
+// of single-thread instructions (MMA, commit) inside warp-uniform code.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // `timeout_ns` of %globaltimer, or until another role of the CTA raised
 // `*abort`. Returns false when it gave up (the caller records the error and

@@ -77,6 +77,7 @@ struct PfParams {
   int rows_per_head;  // 128 / g query positions per tile
   int n_qtiles;       // ceil(T / rows_per_head)
   int n_pairs;        // ceil(n_qtiles / 2)
+  int n_items;        // n_pairs * B * Hkv work items, taken round-robin by the persistent CTAs
   int causal;
   float c;            // scale * log2(e)
   unsigned* err;
@@ -84,15 +85,58 @@ struct PfParams {
 };
 
 struct PfBars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
   uint64_t s_full[2];   // per query tile: S_t(j) computed
   uint64_t p_full[2];   // per query tile: P_t(j) in TMEM (and O_t rescaled)
   uint64_t pv_done[2];  // per query tile: O_t += P_t(j) V_j finished
+  uint64_t o_free[2];   // per query tile: the epilogue has read O_t out of TMEM
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// One work item: a pair of 128-row query tiles of one (batch, KV head).
+struct PfItem {
+  int b, kvh, bh;
+  int p0[2];  // first query position of tile 0 / 1
+  int nj[2];  // key tiles tile 0 / 1 needs (0 for a tile past T)
+};
+
+__device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn) {
+  PfItem w;
+  const int bh_count = p.B * p.Hkv;
+  int qp;
+  if (p.causal) {
+    // items sorted heaviest first, dealt to the CTAs in snake order (rounds of
+    // gridDim.x alternate direction) so that every CTA's total is close to the mean;
+    // the last, partial round keeps the forward direction
+    const int G = gridDim.x;
+    const int round = it / G;
+    const int x = it - round * G;
+    const int sorted = ((round & 1) && (round + 1) * G <= p.n_items) ? round * G + (G - 1 - x) : it;
+    qp = p.n_pairs - 1 - sorted / bh_count;
+    w.bh = sorted % bh_count;
+  } else {  // head-major: CTAs working at the same time share a head's K/V in L2
+    w.bh = it / p.n_pairs;
+    qp = it % p.n_pairs;
+  }
+  w.b = w.bh / p.Hkv;
+  w.kvh = w.bh % p.Hkv;
+  const int shift = p.S - p.T;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int first = (2 * qp + t) * p.rows_per_head;
+    int kv_end = 0;
+    if (first < p.T) {
+      kv_end = p.S;
+      if (p.causal) kv_end = min(p.S, min(first + p.rows_per_head, p.T) - 1 + shift + 1);
+    }
+    w.p0[t] = first;
+    w.nj[t] = kv_end > 0 ? (kv_end + bn - 1) / bn : 0;
+  }
+  return w;
+}
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -109,37 +153,11 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (b, kv head, pair of query tiles); causal runs heaviest pairs first
-  const int bh_count = p.B * p.Hkv;
-  int qp, bh;
-  if (p.causal) {
-    qp = p.n_pairs - 1 - static_cast<int>(blockIdx.x) / bh_count;
-    bh = static_cast<int>(blockIdx.x) % bh_count;
-  } else {
-    bh = static_cast<int>(blockIdx.x) / p.n_pairs;
-    qp = static_cast<int>(blockIdx.x) % p.n_pairs;
-  }
-  const int b = bh / p.Hkv;
-  const int kvh = bh % p.Hkv;
   const int shift = p.S - p.T;  // bottom-right alignment: row i sees keys j <= i + shift
-  // first query position and number of key tiles of query tile t (scalars, not
-  // arrays: a runtime-indexed array would live in local memory)
-  auto tile_nj = [&](int first_pos) -> int {
-    int kv_end = 0;
-    if (first_pos < p.T) {
-      kv_end = p.S;
-      if (p.causal) kv_end = min(p.S, min(first_pos + p.rows_per_head, p.T) - 1 + shift + 1);
-    }
-    return kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
-  };
-  const int p0_0 = (2 * qp) * p.rows_per_head;
-  const int p0_1 = p0_0 + p.rows_per_head;
-  const int nj_0 = tile_nj(p0_0);
-  const int nj_1 = tile_nj(p0_1);
-  const int nj = max(nj_0, nj_1);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
@@ -148,6 +166,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->pv_done[s], 1);
+      mbar_init(&bars->o_free[s], 128);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -171,129 +190,193 @@ __global__ void __launch_bounds__(384, 1)
     warpgroup_reg_dealloc<C::AUX_REGS>();
   if (warp == C::PRODUCER_WARP) {
     // ======================= TMA producer =======================
-    if (lane == 0 && nj > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(&bars->q_full, C::QT * C::Q_BYTES);
-      for (int t = 0; t < 2; ++t)
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, t ? p0_1 : p0_0,
-                      kvh * p.g, b);
-      int issued = 0;
-      for (int j = 0; j < nj; ++j) {
-        const int s = j % C::STAGES;
-        const uint32_t u = j / C::STAGES;
-        if (j >= C::STAGES && !mbar_wait(&bars->k_empty[s], (u - 1) & 1, tmo, abort_flag)) {
+      uint32_t g = 0;  // key tiles loaded so far, over all items (ring position)
+      int item_i = 0;
+      uint32_t q_loads = 0;  // Q loads issued (q_full phases)
+      for (int it = blockIdx.x; it < p.n_items && !*abort_flag; it += gridDim.x, ++item_i) {
+        const PfItem w = pf_item(p, it, C::BN);
+        const int nj = max(w.nj[0], w.nj[1]);
+        // Q of the previous item stays in smem until its last S has been computed
+        if (item_i > 0 && !mbar_wait(&bars->q_empty, (item_i - 1) & 1, tmo, abort_flag)) {
           fail(SITE_PF_PRODUCER);
           break;
         }
-        mbar_arrive_expect_tx(&bars->k_full[s], C::KV_BYTES);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, j * C::BN, bh);
-        if (j >= C::STAGES && !mbar_wait(&bars->v_empty[s], (u - 1) & 1, tmo, abort_flag)) {
-          fail(SITE_PF_PRODUCER);
-          mbar_wait(&bars->k_full[s], u & 1, tmo);  // K_j was issued: let it land
-          break;
+        mbar_arrive_expect_tx(&bars->q_full, C::QT * C::Q_BYTES);
+        for (int t = 0; t < 2; ++t)
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, w.p0[t],
+                        w.kvh * p.g, w.b);
+        ++q_loads;
+        for (int j = 0; j < nj; ++j, ++g) {
+          const int s = g % C::STAGES;
+          const uint32_t u = g / C::STAGES;
+          if (g >= C::STAGES && !mbar_wait(&bars->k_empty[s], (u - 1) & 1, tmo, abort_flag)) {
+            fail(SITE_PF_PRODUCER);
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->k_full[s], C::KV_BYTES);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, j * C::BN,
+                        w.bh);
+          if (g >= C::STAGES && !mbar_wait(&bars->v_empty[s], (u - 1) & 1, tmo, abort_flag)) {
+            fail(SITE_PF_PRODUCER);
+            mbar_wait(&bars->k_full[s], u & 1, tmo);  // K was issued: let it land
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full[s], C::KV_BYTES);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->v_full[s], c * 64, j * C::BN,
+                        w.bh);
         }
-        mbar_arrive_expect_tx(&bars->v_full[s], C::KV_BYTES);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->v_full[s], c * 64, j * C::BN, bh);
-        issued = j + 1;
       }
       if (*abort_flag) {
         // copies still in flight must complete before the CTA exits
-        mbar_wait(&bars->q_full, 0, tmo);
-        for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
-          mbar_wait(&bars->k_full[j % C::STAGES], (j / C::STAGES) & 1, tmo);
-          mbar_wait(&bars->v_full[j % C::STAGES], (j / C::STAGES) & 1, tmo);
+        if (q_loads > 0) mbar_wait(&bars->q_full, (q_loads - 1) & 1, tmo);
+        for (uint32_t x = g > C::STAGES ? g - C::STAGES : 0; x < g; ++x) {
+          mbar_wait(&bars->k_full[x % C::STAGES], (x / C::STAGES) & 1, tmo);
+          mbar_wait(&bars->v_full[x % C::STAGES], (x / C::STAGES) & 1, tmo);
         }
       }
     }
   } else if (warp == C::MMA_WARP) {
     // ======================= MMA issuer =======================
-    if (lane == 0 && nj > 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, C::BN, 0, 0);  // A = Q (K-major), B = K (K-major)
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);      // A = P (TMEM), B = V (MN-major)
-      // descriptors of the operand bases; an MMA adds its (compile-time) byte offset >> 4
-      // to the start-address field, which never carries out of its 14 bits (smem < 256 KB)
-      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV = smem_desc_sw128(smem_u32(sV), C::CHUNK_BYTES, 1024);
-      bool ok = mbar_wait(&bars->q_full, 0, tmo, abort_flag);
-      tc_fence_after();
-      // S_t(j) = Q_t K_j^T into tile t's S/P columns
-      auto qk = [=](int t, int j) {
-        const uint64_t a0 = dQ + static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
-        const uint64_t b0 = dK + static_cast<uint64_t>(((j % C::STAGES) * C::KV_BYTES) >> 4);
-        const uint32_t dS = tmem + t * C::TILE_COLS;
+    // The whole warp runs the loop (waits, descriptors, loop control stay
+    // warp-uniform); one elected lane issues each MMA and commit.
+    const bool leader = elect_one();
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, C::BN, 0, 0);  // A = Q (K-major), B = K (K-major)
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);      // A = P (TMEM), B = V (MN-major)
+    // descriptors of the operand bases; an MMA adds its (compile-time) byte offset >> 4
+    // to the start-address field, which never carries out of its 14 bits (smem < 256 KB)
+    const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t dV = smem_desc_sw128(smem_u32(sV), C::CHUNK_BYTES, 1024);
+    // S_t = Q_t K^T (K in ring stage st) into tile t's S/P columns
+    auto qk = [=](int t, int st) {
+      const uint64_t a0 = dQ + static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
+      const uint64_t b0 = dK + static_cast<uint64_t>((st * C::KV_BYTES) >> 4);
+      const uint32_t dS = tmem + t * C::TILE_COLS;
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // 16 elements of d per MMA: chunk kk/4, 32-byte step inside the 128-byte swizzle row
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
           tc_mma_ss(dS, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
-      };
-      // O_t += P_t(j) V_j: P from TMEM (8 columns = 16 keys per MMA), V MN-major from smem
-      auto pv = [=](int t, int j) {
-        const uint64_t b0 = dV + static_cast<uint64_t>(((j % C::STAGES) * C::KV_BYTES) >> 4);
-        const uint32_t dO = tmem + t * C::TILE_COLS + C::O_OFF;
-        const uint32_t aP = tmem + t * C::TILE_COLS;
+      }
+      __syncwarp();
+    };
+    // O_t (+)= P_t V (V in ring stage st): P from TMEM (8 columns = 16 keys per MMA),
+    // V MN-major from smem; the first key tile of an item overwrites O
+    auto pv = [=](int t, int st, bool first) {
+      const uint64_t b0 = dV + static_cast<uint64_t>((st * C::KV_BYTES) >> 4);
+      const uint32_t dO = tmem + t * C::TILE_COLS + C::O_OFF;
+      const uint32_t aP = tmem + t * C::TILE_COLS;
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           tc_mma_ts(dO, aP + kk * 8, b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-      };
-      if (ok) {
-        ok = mbar_wait(&bars->k_full[0], 0, tmo, abort_flag);
-        tc_fence_after();
-        if (ok) {
-          for (int t = 0; t < 2; ++t)
-            if ((t ? nj_1 : nj_0) > 0) {
-              qk(t, 0);
-              tc_commit(&bars->s_full[t]);
-            }
-          tc_commit(&bars->k_empty[0]);
-        }
+                    (!first || kk > 0) ? 1u : 0u);
       }
+      __syncwarp();
+    };
+    auto commit = [=](uint64_t* bar) {
+      if (leader) tc_commit(bar);
+      __syncwarp();
+    };
+    // waits are warp-collective: every lane sees the same outcome
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, tmo, abort_flag));
+    };
+    bool ok = true;
+    uint32_t g = 0;                 // key tiles consumed so far, over all items (ring position)
+    uint32_t pc0 = 0, pc1 = 0;      // key tiles of tile 0 / 1 done so far (s_full / p_full / pv_done phases)
+    uint32_t ep0 = 0, ep1 = 0;      // items whose epilogue reads O_0 / O_1 (o_free phases)
+    int item_i = 0;
+    for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++item_i) {
+      const PfItem w = pf_item(p, it, C::BN);
+      const int nj0 = w.nj[0], nj1 = w.nj[1];
+      const int nj = max(nj0, nj1);
+      if (!wwait(&bars->q_full, item_i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (nj == 0) {
+        if (leader) mbar_arrive(&bars->q_empty);  // nothing read Q
+        __syncwarp();
+        continue;
+      }
+      if (!wwait(&bars->k_full[g % C::STAGES], (g / C::STAGES) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (nj0 > 0) {
+        qk(0, g % C::STAGES);
+        commit(&bars->s_full[0]);
+      }
+      if (nj1 > 0) {
+        qk(1, g % C::STAGES);
+        commit(&bars->s_full[1]);
+      }
+      commit(&bars->k_empty[g % C::STAGES]);
+      if (nj == 1) commit(&bars->q_empty);  // that was this item's last S
       for (int j = 0; ok && j < nj; ++j) {
-        const int s = j % C::STAGES;
+        const uint32_t gj = g + j;
+        const int s = gj % C::STAGES;
         bool k_next_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int njt = t ? nj_1 : nj_0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int njt = t ? nj1 : nj0;
           if (j >= njt) continue;
-          if (!mbar_wait(&bars->p_full[t], j & 1, tmo, abort_flag) ||
-              !mbar_wait(&bars->v_full[s], (j / C::STAGES) & 1, tmo, abort_flag)) {
+          const uint32_t pc = t ? pc1 : pc0;
+          const uint32_t ep = t ? ep1 : ep0;
+          if (!wwait(&bars->p_full[t], pc & 1) || !wwait(&bars->v_full[s], (gj / C::STAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          // the first PV of an item overwrites O_t: the previous item's epilogue must have read it
+          if (j == 0 && ep > 0 && !wwait(&bars->o_free[t], (ep - 1) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          pv(t, j);
-          tc_commit(&bars->pv_done[t]);
-          // the next S of this tile overwrites the columns P_t(j) is read from; MMAs
+          pv(t, s, j == 0);
+          commit(&bars->pv_done[t]);
+          if (t) ++pc1; else ++pc0;
+          // the next S of this tile overwrites the columns P_t is read from; MMAs
           // issued by one thread execute in order, so it is queued right behind
           if (j + 1 < njt) {
+            const uint32_t g1 = gj + 1;
             if (!k_next_ready) {
-              if (!mbar_wait(&bars->k_full[(j + 1) % C::STAGES], ((j + 1) / C::STAGES) & 1, tmo, abort_flag)) {
+              if (!wwait(&bars->k_full[g1 % C::STAGES], (g1 / C::STAGES) & 1)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               k_next_ready = true;
             }
-            qk(t, j + 1);
-            tc_commit(&bars->s_full[t]);
+            qk(t, g1 % C::STAGES);
+            commit(&bars->s_full[t]);
           }
         }
         if (!ok) break;
-        tc_commit(&bars->v_empty[s]);
-        if (k_next_ready) tc_commit(&bars->k_empty[(j + 1) % C::STAGES]);
+        commit(&bars->v_empty[s]);
+        if (k_next_ready) commit(&bars->k_empty[(gj + 1) % C::STAGES]);
+        if (j + 2 == nj) commit(&bars->q_empty);  // the item's last S was just issued
       }
-      if (!ok) fail(SITE_PF_MMA);
-      // every MMA issued must finish before TMEM is released
-      tc_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, tmo);
+      if (nj0 > 0) ++ep0;
+      if (nj1 > 0) ++ep1;
+      g += nj;
     }
+    if (!ok && leader) fail(SITE_PF_MMA);
+    // every MMA issued must finish before TMEM is released
+    commit(&bars->drain);
+    mbar_wait(&bars->drain, 0, tmo);
   }
   } else {
     // ======================= softmax: warps 0-3 (tile 0), 4-7 (tile 1) =======================
@@ -301,14 +384,9 @@ __global__ void __launch_bounds__(384, 1)
     const int t = warp >> 2;
     const int r = threadIdx.x & 127;  // row of the tile == TMEM lane
     const int h_local = r / p.rows_per_head;
-    const int my_p0 = t ? p0_1 : p0_0;
-    const int pos = my_p0 + (r % p.rows_per_head);
-    const bool row_valid = pos < p.T;
-    const int vis_last = pos + shift;  // causal: last visible key of this row
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * C::TILE_COLS;
     const uint32_t tO = tS + C::O_OFF;
-    const int my_nj = t ? nj_1 : nj_0;
     const float c = p.c;
     const float2 c2 = make_float2(c, c);
     // m: the row's reference max, in units of log2 (scores times c); l: the running
@@ -319,8 +397,6 @@ __global__ void __launch_bounds__(384, 1)
     // <= 2^kRescaleSlack. Every term then carries the same constant factor,
     // which O / l cancels, so the result is the same softmax.
     constexpr float kRescaleSlack = 8.f;
-    float m = -INFINITY;
-    float l = 0.f;
     bool ok = true;
     // waits are warp-collective: the warp leaves together, so the .sync.aligned
     // tcgen05 loads and the votes below always see all 32 lanes
@@ -328,133 +404,150 @@ __global__ void __launch_bounds__(384, 1)
       const bool w = mbar_wait(bar, parity, tmo, abort_flag);
       return __all_sync(0xffffffffu, w);
     };
+    uint32_t cnt = 0;  // key tiles of this query tile done so far, over all items (barrier phases)
+    for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
+      const PfItem w = pf_item(p, it, C::BN);
+      // selects, not a runtime index into w (which would put w in local memory)
+      const int my_nj = t ? w.nj[1] : w.nj[0];
+      const int my_p0 = t ? w.p0[1] : w.p0[0];
+      const int pos = my_p0 + (r % p.rows_per_head);
+      const bool row_valid = pos < p.T;
+      const int vis_last = pos + shift;  // causal: last visible key of this row
+      float m = -INFINITY;
+      float l = 0.f;
 
-    for (int j = 0; j < my_nj; ++j) {
-      if (!wwait(&bars->s_full[t], j & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // S row: four 32-column loads in flight, one wait
-      uint32_t raw[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, raw[cc]);
-      tmem_ld_wait();
-      float s[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
-
-      const int key0 = j * C::BN;
-      const bool need_mask = (key0 + C::BN > p.S) || (p.causal && key0 + C::BN - 1 > my_p0 + shift);
-      if (need_mask) {
-        const int lim = (p.causal ? min(p.S - 1, vis_last) : p.S - 1) - key0;
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i > lim) s[i] = -INFINITY;
-      }
-      // row max: eight independent three-input chains, then a short tree
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float a = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
-#pragma unroll
-        for (int i = 3; i < 15; i += 2) a = fmax3(a, s[16 * k + i], s[16 * k + i + 1]);
-        mx8[k] = fmaxf(a, s[16 * k + 15]);
-      }
-      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-      const float m_tile = mx * c;
-      const float m_new = (m_tile > m + kRescaleSlack) ? m_tile : m;  // m = -inf: first visible key sets it
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);  // 1 if the reference is kept; 0 while nothing was seen
-      // p = 2^(s*c - m): packed FFMA, MUFU ex2, bf16 pairs stored over S, 32 columns at a time
-      const float2 nm2 = make_float2(-m_use, -m_use);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = cc * 32 + 2 * i;
-          const float2 x = ffma2(make_float2(s[e], s[e + 1]), c2, nm2);
-          const float2 ev = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[i & 3] = fadd2(acc[i & 3], ev);
-          pk[i] = pack_bf16x2(ev.x, ev.y);
-        }
-        tmem_st16(tS + cc * 16, pk);  // keys 32cc .. 32cc+31 -> columns 16cc .. 16cc+15
-      }
-      const float2 a01 = fadd2(acc[0], acc[1]);
-      const float2 a23 = fadd2(acc[2], acc[3]);
-      const float2 at = fadd2(a01, a23);
-      l = fmaf(l, alpha, at.x + at.y);
-      m = m_new;
-
-      // O is rescaled only when the max of some row of this warp rose; that
-      // needs PV_t(j-1) finished (it accumulates into O)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!wwait(&bars->pv_done[t], (j - 1) & 1)) {
+      for (int j = 0; j < my_nj; ++j, ++cnt) {
+        if (!wwait(&bars->s_full[t], cnt & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float2 al2 = make_float2(alpha, alpha);
+        // S row: four 32-column loads in flight, one wait
+        uint32_t raw[4][32];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; cc += 2) {
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tO + cc * 32, o0);
-          tmem_ld32(tO + cc * 32 + 32, o1);
-          tmem_ld_wait();
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, raw[cc]);
+        tmem_ld_wait();
+        float s[128];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float2 v0 = fmul2(make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), al2);
-            float2 v1 = fmul2(make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), al2);
-            o0[i] = __float_as_uint(v0.x);
-            o0[i + 1] = __float_as_uint(v0.y);
-            o1[i] = __float_as_uint(v1.x);
-            o1[i + 1] = __float_as_uint(v1.y);
-          }
-          tmem_st32(tO + cc * 32, o0);
-          tmem_st32(tO + cc * 32 + 32, o1);
-        }
-      }
-      tmem_st_wait();  // P (and O) stores complete before the MMA may read them
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
-    }
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
 
-    // ---- epilogue: O / l -> bf16, lse = ln2 * (m + log2 l)
-    if (ok && my_nj > 0) {
-      if (!wwait(&bars->pv_done[t], (my_nj - 1) & 1)) ok = false;
-      tc_fence_after();
-    }
-    if (!ok) fail(SITE_PF_SOFTMAX);
-    const int h = kvh * p.g + h_local;
-    const size_t row_index = (static_cast<size_t>(b) * p.Hq + h) * p.T + pos;
-    __nv_bfloat16* orow = p.o + row_index * D;
-    if (ok) {
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const int key0 = j * C::BN;
+        const bool need_mask = (key0 + C::BN > p.S) || (p.causal && key0 + C::BN - 1 > my_p0 + shift);
+        if (need_mask) {
+          const int lim = (p.causal ? min(p.S - 1, vis_last) : p.S - 1) - key0;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        if (my_nj > 0) {
-          tmem_ld32(tO + cc * 32, o);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int i = 0; i < 128; ++i)
+            if (i > lim) s[i] = -INFINITY;
         }
-        if (row_valid) {
+        // row max: eight independent three-input chains, then a short tree
+        float mx8[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + cc * 32 + 8 * q) = v;
+        for (int k = 0; k < 8; ++k) {
+          float a = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
+#pragma unroll
+          for (int i = 3; i < 15; i += 2) a = fmax3(a, s[16 * k + i], s[16 * k + i + 1]);
+          mx8[k] = fmaxf(a, s[16 * k + 15]);
+        }
+        const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+        const float m_tile = mx * c;
+        const float m_new = (m_tile > m + kRescaleSlack) ? m_tile : m;  // m = -inf: first visible key sets it
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2_approx(m - m_use);  // 1 if the reference is kept; 0 while nothing was seen
+        // p = 2^(s*c - m): packed FFMA, MUFU ex2, bf16 pairs stored over S, 32 columns at a time
+        const float2 nm2 = make_float2(-m_use, -m_use);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int e = cc * 32 + 2 * i;
+            const float2 x = ffma2(make_float2(s[e], s[e + 1]), c2, nm2);
+            const float2 ev = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            acc[i & 3] = fadd2(acc[i & 3], ev);
+            pk[i] = pack_bf16x2(ev.x, ev.y);
+          }
+          tmem_st16(tS + cc * 16, pk);  // keys 32cc .. 32cc+31 -> columns 16cc .. 16cc+15
+        }
+        const float2 a01 = fadd2(acc[0], acc[1]);
+        const float2 a23 = fadd2(acc[2], acc[3]);
+        const float2 at = fadd2(a01, a23);
+        l = fmaf(l, alpha, at.x + at.y);
+        m = m_new;
+
+        // O is rescaled only when the max of some row of this warp rose; that
+        // needs PV_t(j-1) finished (it accumulates into O)
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!wwait(&bars->pv_done[t], (cnt - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; cc += 2) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tO + cc * 32, o0);
+            tmem_ld32(tO + cc * 32 + 32, o1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float2 v0 = fmul2(make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), al2);
+              float2 v1 = fmul2(make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), al2);
+              o0[i] = __float_as_uint(v0.x);
+              o0[i + 1] = __float_as_uint(v0.y);
+              o1[i] = __float_as_uint(v1.x);
+              o1[i + 1] = __float_as_uint(v1.y);
+            }
+            tmem_st32(tO + cc * 32, o0);
+            tmem_st32(tO + cc * 32 + 32, o1);
           }
         }
+        tmem_st_wait();  // P (and O) stores complete before the MMA may read them
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
       }
-      if (row_valid && p.lse) p.lse[row_index] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+
+      // ---- epilogue: O / l -> bf16, lse = ln2 * (m + log2 l)
+      if (ok && my_nj > 0) {
+        if (!wwait(&bars->pv_done[t], (cnt - 1) & 1)) ok = false;
+        tc_fence_after();
+      }
+      if (!ok) fail(SITE_PF_SOFTMAX);
+      const int h = w.kvh * p.g + h_local;
+      const size_t row_index = (static_cast<size_t>(w.b) * p.Hq + h) * p.T + pos;
+      __nv_bfloat16* orow = p.o + row_index * D;
+      if (ok) {
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          if (my_nj > 0) {
+            tmem_ld32(tO + cc * 32, o);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (row_valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + cc * 32 + 8 * q) = v;
+            }
+          }
+        }
+        if (row_valid && p.lse) p.lse[row_index] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      }
+      // O_t has been read out: the next item's first PV may overwrite it
+      if (ok && my_nj > 0) {
+        tc_fence_before();
+        mbar_arrive(&bars->o_free[t]);
+      }
     }
   }
 
@@ -473,6 +566,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();  // defined in api.cu
+int device_sm_count();              // defined in api.cu
 
 int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                       int T, int S, int d, float scale, int causal, cudaStream_t stream, unsigned* err,
@@ -518,18 +612,23 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, floa
   p.c = scale * kLog2e;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  const long long grid = static_cast<long long>(p.n_pairs) * B * Hkv;
-  if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const long long items = static_cast<long long>(p.n_pairs) * B * Hkv;
+  if (items > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  p.n_items = static_cast<int>(items);
+  // persistent: one CTA per SM, each takes items blockIdx.x, blockIdx.x + grid, ...
+  const int sms = device_sm_count();
+  if (sms <= 0) return FA_ERR_CUDA;
+  const int grid = items < sms ? static_cast<int>(items) : sms;
   if (d == 128) {
     auto kfn = prefill_tc_kernel<128>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<128>::SMEM) != cudaSuccess)
       return FA_ERR_CUDA;
-    kfn<<<static_cast<unsigned>(grid), PfCfg<128>::THREADS, PfCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
+    kfn<<<grid, PfCfg<128>::THREADS, PfCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
   } else {
     auto kfn = prefill_tc_kernel<64>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<64>::SMEM) != cudaSuccess)
       return FA_ERR_CUDA;
-    kfn<<<static_cast<unsigned>(grid), PfCfg<64>::THREADS, PfCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
+    kfn<<<grid, PfCfg<64>::THREADS, PfCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
   }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

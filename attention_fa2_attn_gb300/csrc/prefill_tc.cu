@@ -89,7 +89,7 @@ struct PfBars {
   uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
   uint64_t s_full[2];   // per query tile: S_t(j) computed
   uint64_t p_full[2];   // per query tile: P_t(j) in TMEM (and O_t rescaled)
-  uint64_t pv_done[2];  // per query tile: O_t += P_t(j) V_j finished
+  uint64_t pv_done[2];  // per query tile: the item's last O_t += P_t V finished (once per item)
   uint64_t o_free[2];   // per query tile: the epilogue has read O_t out of TMEM
   uint64_t drain;
   uint32_t tmem_base;
@@ -287,13 +287,12 @@ __global__ void __launch_bounds__(384, 1)
       if (leader) tc_commit(bar);
       __syncwarp();
     };
-    // waits are warp-collective: every lane sees the same outcome
-    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, tmo, abort_flag));
-    };
+    // every lane polls the same barrier and the same timer in the same
+    // instruction, so the outcome is warp-uniform without a vote
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool { return mbar_wait(bar, parity, tmo, abort_flag); };
     bool ok = true;
     uint32_t g = 0;                 // key tiles consumed so far, over all items (ring position)
-    uint32_t pc0 = 0, pc1 = 0;      // key tiles of tile 0 / 1 done so far (s_full / p_full / pv_done phases)
+    uint32_t pc0 = 0, pc1 = 0;      // key tiles of tile 0 / 1 done so far (p_full phases)
     uint32_t ep0 = 0, ep1 = 0;      // items whose epilogue reads O_0 / O_1 (o_free phases)
     int item_i = 0;
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++item_i) {
@@ -328,6 +327,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; ok && j < nj; ++j) {
         const uint32_t gj = g + j;
         const int s = gj % C::STAGES;
+        bool v_ready = false;
         bool k_next_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -335,9 +335,16 @@ __global__ void __launch_bounds__(384, 1)
           if (j >= njt) continue;
           const uint32_t pc = t ? pc1 : pc0;
           const uint32_t ep = t ? ep1 : ep0;
-          if (!wwait(&bars->p_full[t], pc & 1) || !wwait(&bars->v_full[s], (gj / C::STAGES) & 1)) {
+          if (!wwait(&bars->p_full[t], pc & 1)) {
             ok = false;
             break;
+          }
+          if (!v_ready) {
+            if (!wwait(&bars->v_full[s], (gj / C::STAGES) & 1)) {
+              ok = false;
+              break;
+            }
+            v_ready = true;
           }
           // the first PV of an item overwrites O_t: the previous item's epilogue must have read it
           if (j == 0 && ep > 0 && !wwait(&bars->o_free[t], (ep - 1) & 1)) {
@@ -346,8 +353,12 @@ __global__ void __launch_bounds__(384, 1)
           }
           tc_fence_after();
           pv(t, s, j == 0);
-          commit(&bars->pv_done[t]);
           if (t) ++pc1; else ++pc0;
+          // the epilogue waits for the item's last PV; a rescale of O at step j needs
+          // PV_t(j-1) finished, which the s_full commit of S_t(j) (issued after it) implies
+          if (j + 1 == njt) commit(&bars->pv_done[t]);
+          // V_j is free once its last reader has run
+          if (t == 1 || j >= nj1) commit(&bars->v_empty[s]);
           // the next S of this tile overwrites the columns P_t is read from; MMAs
           // issued by one thread execute in order, so it is queued right behind
           if (j + 1 < njt) {
@@ -365,7 +376,6 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (!ok) break;
-        commit(&bars->v_empty[s]);
         if (k_next_ready) commit(&bars->k_empty[(gj + 1) % C::STAGES]);
         if (j + 2 == nj) commit(&bars->q_empty);  // the item's last S was just issued
       }
@@ -404,7 +414,8 @@ __global__ void __launch_bounds__(384, 1)
       const bool w = mbar_wait(bar, parity, tmo, abort_flag);
       return __all_sync(0xffffffffu, w);
     };
-    uint32_t cnt = 0;  // key tiles of this query tile done so far, over all items (barrier phases)
+    uint32_t cnt = 0;   // key tiles of this query tile done so far, over all items (s_full phases)
+    uint32_t ecnt = 0;  // items of this query tile with at least one key tile (pv_done phases)
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
       const PfItem w = pf_item(p, it, C::BN);
       // selects, not a runtime index into w (which would put w in local memory)
@@ -476,13 +487,9 @@ __global__ void __launch_bounds__(384, 1)
         m = m_new;
 
         // O is rescaled only when the max of some row of this warp rose; that
-        // needs PV_t(j-1) finished (it accumulates into O)
+        // needs PV_t(j-1) finished (it accumulates into O), which S_t(j) being
+        // complete already implies: its commit was issued after that PV
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wwait(&bars->pv_done[t], (cnt - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
           for (int cc = 0; cc < D / 32; cc += 2) {
@@ -510,7 +517,8 @@ __global__ void __launch_bounds__(384, 1)
 
       // ---- epilogue: O / l -> bf16, lse = ln2 * (m + log2 l)
       if (ok && my_nj > 0) {
-        if (!wwait(&bars->pv_done[t], (cnt - 1) & 1)) ok = false;
+        if (!wwait(&bars->pv_done[t], ecnt & 1)) ok = false;
+        ++ecnt;
         tc_fence_after();
       }
       if (!ok) fail(SITE_PF_SOFTMAX);

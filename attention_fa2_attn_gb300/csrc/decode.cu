@@ -428,8 +428,13 @@ __global__ void __launch_bounds__(160, PAGED ? 2 : 1)
 }
 
 // ---------------------------------------------------------------------------
-// LSE merge: one warp per output row
+// LSE merge: one warp per (output row, 32-column slice)
 // ---------------------------------------------------------------------------
+// lse = ln sum_s e^{lse_s};  O = sum_s e^{lse_s - lse} O_s. Each warp reduces the
+// row's lse over the splits itself (the lse_part reads are tiny and L2 resident);
+// the weights of 32 splits at a time sit one per lane and are broadcast by
+// shuffle, so a lane's loads of O_s for its column are independent of one
+// another and several are in flight at once.
 __global__ void __launch_bounds__(128) lse_merge_kernel(const float* __restrict__ o_part,
                                                         const float* __restrict__ lse_part,
                                                         __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
@@ -438,8 +443,11 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float* __restrict_
   // has finished and its partials are visible (a no-op for a plain launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
-  if (row >= rows) return;
+  const int slices = (d + 31) >> 5;
+  const long long gw = static_cast<long long>(blockIdx.x) * 4 + warp;
+  if (gw >= static_cast<long long>(rows) * slices) return;
+  const int row = static_cast<int>(gw / slices);
+  const int col = static_cast<int>(gw % slices) * 32 + lane;
   float mx = -INFINITY;
   for (int s = lane; s < n; s += 32) mx = fmaxf(mx, lse_part[static_cast<size_t>(s) * rows + row]);
 #pragma unroll
@@ -453,28 +461,26 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float* __restrict_
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
   const float lrow = (mx == -INFINITY) ? -INFINITY : mx + logf(tot);
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  float acc = 0.f;
   if (mx != -INFINITY) {
-    for (int s = 0; s < n; ++s) {
-      const float ls = lse_part[static_cast<size_t>(s) * rows + row];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - lrow);
-      const float* src = o_part + (static_cast<size_t>(s) * rows + row) * d;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int col = lane + 32 * i;
-        if (col < d) acc[i] = fmaf(w, src[col], acc[i]);
+    for (int s0 = 0; s0 < n; s0 += 32) {
+      float ws = 0.f;  // weight of split s0 + lane; 0 for an empty split (its O_s is never read)
+      if (s0 + lane < n) {
+        const float ls = lse_part[static_cast<size_t>(s0 + lane) * rows + row];
+        if (ls != -INFINITY) ws = expf(ls - lrow);
+      }
+      const int cnt = min(32, n - s0);
+      const float* src = o_part + (static_cast<size_t>(s0) * rows + row) * d + col;
+      const size_t step = static_cast<size_t>(rows) * d;
+#pragma unroll 8
+      for (int i = 0; i < cnt; ++i) {
+        const float w = __shfl_sync(0xffffffffu, ws, i);
+        if (w != 0.f && col < d) acc = fmaf(w, src[i * step], acc);
       }
     }
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int col = lane + 32 * i;
-    if (col < d) o[static_cast<size_t>(row) * d + col] = __float2bfloat16_rn(acc[i]);
-  }
-  if (lse && lane == 0) lse[row] = lrow;
+  if (col < d) o[static_cast<size_t>(row) * d + col] = __float2bfloat16_rn(acc);
+  if (lse && gw % slices == 0 && lane == 0) lse[row] = lrow;
 }
 
 // ---------------------------------------------------------------------------
@@ -492,7 +498,9 @@ constexpr int dec_stages() { return PAGED ? 3 : 4; }
 // programmatic dependent (its launch overlaps the split kernel's tail).
 static int launch_lse_merge_impl(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows,
                                  int d, cudaStream_t stream, bool after_split) {
-  const int grid = (rows + 3) / 4;
+  const long long warps = static_cast<long long>(rows) * ((d + 31) / 32);
+  if ((warps + 3) / 4 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const int grid = static_cast<int>((warps + 3) / 4);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(128);

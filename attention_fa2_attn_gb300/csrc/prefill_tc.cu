@@ -90,7 +90,6 @@ struct PfBars {
   uint64_t s_full[2];   // per query tile: S_t(j) computed
   uint64_t p_full[2];   // per query tile: P_t(j) in TMEM (and O_t rescaled)
   uint64_t pv_done[2];  // per query tile: the item's last O_t += P_t V finished (once per item)
-  uint64_t o_free[2];   // per query tile: the epilogue has read O_t out of TMEM
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -166,7 +165,6 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->pv_done[s], 1);
-      mbar_init(&bars->o_free[s], 128);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -267,7 +265,6 @@ __global__ void __launch_bounds__(384, 1)
           tc_mma_ss(dS, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       }
-      __syncwarp();
     };
     // O_t (+)= P_t V (V in ring stage st): P from TMEM (8 columns = 16 keys per MMA),
     // V MN-major from smem; the first key tile of an item overwrites O
@@ -281,19 +278,16 @@ __global__ void __launch_bounds__(384, 1)
           tc_mma_ts(dO, aP + kk * 8, b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
                     (!first || kk > 0) ? 1u : 0u);
       }
-      __syncwarp();
     };
     auto commit = [=](uint64_t* bar) {
       if (leader) tc_commit(bar);
-      __syncwarp();
     };
     // every lane polls the same barrier and the same timer in the same
     // instruction, so the outcome is warp-uniform without a vote
     auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool { return mbar_wait(bar, parity, tmo, abort_flag); };
     bool ok = true;
-    uint32_t g = 0;                 // key tiles consumed so far, over all items (ring position)
-    uint32_t pc0 = 0, pc1 = 0;      // key tiles of tile 0 / 1 done so far (p_full phases)
-    uint32_t ep0 = 0, ep1 = 0;      // items whose epilogue reads O_0 / O_1 (o_free phases)
+    uint32_t g = 0;                // key tiles consumed so far, over all items (ring position)
+    uint32_t pph0 = 0, pph1 = 0;   // p_full phase parity of tile 0 / 1
     int item_i = 0;
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++item_i) {
       const PfItem w = pf_item(p, it, C::BN);
@@ -306,81 +300,86 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       if (nj == 0) {
         if (leader) mbar_arrive(&bars->q_empty);  // nothing read Q
-        __syncwarp();
         continue;
       }
-      if (!wwait(&bars->k_full[g % C::STAGES], (g / C::STAGES) & 1)) {
+      if (!wwait(&bars->k_full[g & 1], (g >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (nj0 > 0) {
-        qk(0, g % C::STAGES);
+        qk(0, g & 1);
         commit(&bars->s_full[0]);
       }
       if (nj1 > 0) {
-        qk(1, g % C::STAGES);
+        qk(1, g & 1);
         commit(&bars->s_full[1]);
       }
-      commit(&bars->k_empty[g % C::STAGES]);
+      commit(&bars->k_empty[g & 1]);
       if (nj == 1) commit(&bars->q_empty);  // that was this item's last S
-      for (int j = 0; ok && j < nj; ++j) {
+      static_assert(C::STAGES == 2, "the issue loop below indexes a two-stage K/V ring");
+      // K/V ring of two stages: key tile x sits in stage x & 1, phase (x >> 1) & 1.
+      // The first PV of an item overwrites O_t; the softmax threads read O_t out
+      // for the previous item before they publish this item's first P_t, so the
+      // P wait orders it. A rescale of O at step j needs PV_t(j-1) finished, which
+      // the S_t(j) commit (issued after it) implies, so pv_done is per item.
+      for (int j = 0; j < nj; ++j) {
         const uint32_t gj = g + j;
-        const int s = gj % C::STAGES;
-        bool v_ready = false;
-        bool k_next_ready = false;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int njt = t ? nj1 : nj0;
-          if (j >= njt) continue;
-          const uint32_t pc = t ? pc1 : pc0;
-          const uint32_t ep = t ? ep1 : ep0;
-          if (!wwait(&bars->p_full[t], pc & 1)) {
+        const int s = gj & 1;                       // V_j (and K_j)
+        const uint32_t vph = (gj >> 1) & 1;
+        const int s1 = s ^ 1;                       // K_{j+1}
+        const uint32_t kph1 = ((gj + 1) >> 1) & 1;
+        bool k_ready = false;
+        // ---- tile 0
+        if (j < nj0) {
+          if (!wwait(&bars->p_full[0], pph0) || !wwait(&bars->v_full[s], vph)) {
             ok = false;
             break;
           }
-          if (!v_ready) {
-            if (!wwait(&bars->v_full[s], (gj / C::STAGES) & 1)) {
+          pph0 ^= 1;
+          tc_fence_after();
+          pv(0, s, j == 0);
+          if (j + 1 == nj0) commit(&bars->pv_done[0]);
+          if (j >= nj1) commit(&bars->v_empty[s]);  // tile 1 does not read V_j
+          // the next S of this tile overwrites the columns P_0 is read from; MMAs
+          // issued by one thread execute in order, so it is queued right behind
+          if (j + 1 < nj0) {
+            if (!wwait(&bars->k_full[s1], kph1)) {
               ok = false;
               break;
             }
-            v_ready = true;
+            tc_fence_after();
+            k_ready = true;
+            qk(0, s1);
+            commit(&bars->s_full[0]);
           }
-          // the first PV of an item overwrites O_t: the previous item's epilogue must have read it
-          if (j == 0 && ep > 0 && !wwait(&bars->o_free[t], (ep - 1) & 1)) {
+        }
+        // ---- tile 1
+        if (j < nj1) {
+          if (!wwait(&bars->p_full[1], pph1) || (j >= nj0 && !wwait(&bars->v_full[s], vph))) {
             ok = false;
             break;
           }
+          pph1 ^= 1;
           tc_fence_after();
-          pv(t, s, j == 0);
-          if (t) ++pc1; else ++pc0;
-          // the epilogue waits for the item's last PV; a rescale of O at step j needs
-          // PV_t(j-1) finished, which the s_full commit of S_t(j) (issued after it) implies
-          if (j + 1 == njt) commit(&bars->pv_done[t]);
-          // V_j is free once its last reader has run
-          if (t == 1 || j >= nj1) commit(&bars->v_empty[s]);
-          // the next S of this tile overwrites the columns P_t is read from; MMAs
-          // issued by one thread execute in order, so it is queued right behind
-          if (j + 1 < njt) {
-            const uint32_t g1 = gj + 1;
-            if (!k_next_ready) {
-              if (!wwait(&bars->k_full[g1 % C::STAGES], (g1 / C::STAGES) & 1)) {
+          pv(1, s, j == 0);
+          if (j + 1 == nj1) commit(&bars->pv_done[1]);
+          commit(&bars->v_empty[s]);
+          if (j + 1 < nj1) {
+            if (!k_ready) {
+              if (!wwait(&bars->k_full[s1], kph1)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              k_next_ready = true;
             }
-            qk(t, g1 % C::STAGES);
-            commit(&bars->s_full[t]);
+            qk(1, s1);
+            commit(&bars->s_full[1]);
           }
         }
-        if (!ok) break;
-        if (k_next_ready) commit(&bars->k_empty[(gj + 1) % C::STAGES]);
+        if (j + 1 < nj) commit(&bars->k_empty[s1]);
         if (j + 2 == nj) commit(&bars->q_empty);  // the item's last S was just issued
       }
-      if (nj0 > 0) ++ep0;
-      if (nj1 > 0) ++ep1;
       g += nj;
     }
     if (!ok && leader) fail(SITE_PF_MMA);
@@ -551,11 +550,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (row_valid && p.lse) p.lse[row_index] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       }
-      // O_t has been read out: the next item's first PV may overwrite it
-      if (ok && my_nj > 0) {
-        tc_fence_before();
-        mbar_arrive(&bars->o_free[t]);
-      }
+      // O_t has been read out (the loads above completed); these threads arrive on
+      // p_full for the next item only after this, so the MMA warp's wait for that P
+      // also orders the next item's first PV (which overwrites O_t) after these reads
+      if (ok && my_nj > 0) tc_fence_before();
     }
   }
 

@@ -70,8 +70,9 @@ def fa_decode_workspace_bytes(B: int, Hq: int, T: int, d: int, num_splits: int) 
     return int(lib().fa_decode_workspace_bytes(B, Hq, T, d, num_splits))
 
 
-def _resolve_splits(num_splits: int, B: int, Hkv: int, S: int, device) -> int:
-    if num_splits:
+def _resolve_splits(num_splits: int, B: int, Hq: int, Hkv: int, T: int, S: int, device) -> int:
+    if num_splits or (Hq // Hkv) * T > 16:
+        # more than 16 stacked query rows run on the prefill kernel, without a key split
         return int(num_splits)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     return fa_num_splits_heuristic(B, Hkv, S, sms)
@@ -96,7 +97,7 @@ def fa_decode_splitkv(q, k, v, causal: bool = True, num_splits: int = 0, scale: 
     B, Hq, T, d = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    n = _resolve_splits(num_splits, B, Hkv, S, q.device)
+    n = _resolve_splits(num_splits, B, Hq, Hkv, T, S, q.device)
     ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
     o = torch.empty_like(q) if out is None else out
     if lse is None:
@@ -151,7 +152,7 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = Tr
     P, page_size, Hkv, _ = k_pages.shape
     max_pages = block_table.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    n = _resolve_splits(num_splits, B, Hkv, max_pages * page_size, q.device)
+    n = _resolve_splits(num_splits, B, Hq, Hkv, T, max_pages * page_size, q.device)
     ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
     o = torch.empty_like(q) if out is None else out
     if lse is None:

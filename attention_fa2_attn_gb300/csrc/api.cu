@@ -17,7 +17,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                       int T, int S, int d, float scale, int causal, cudaStream_t stream, unsigned* err,
-                      unsigned long long timeout_ns);
+                      unsigned long long timeout_ns, const int* block_table, const int* seqlens, int max_pages,
+                      int num_pages);
 int launch_prefill_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq, int Hkv,
                        int T, int S, int d, float scale, int causal, cudaStream_t stream);
 int launch_decode(const void* q, const void* k, const void* v, const int* block_table, const int* seqlens, void* o,
@@ -160,7 +161,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   unsigned* err = error_word();
   if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
   int rc = launch_prefill_tc(q, k, v, o, lse, B, Hq, Hkv, Tq, Skv, d, scale, causal ? 1 : 0,
-                             static_cast<cudaStream_t>(stream), err, g_timeout_ns);
+                             static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0);
   if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
   return static_cast<fa_status>(rc);
 }
@@ -185,8 +186,20 @@ static fa_status check_decode_common(const void* q, const void* o, int B, int Hq
   if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || Hq % Hkv != 0 || !good_scale(scale)) return FA_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > 1024) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if ((Hq / Hkv) * T > 16) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Hkv > 65535) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq * T >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// More than 16 stacked query rows per KV head (g * T > 16: chunked prefill or a
+// multi-token decode step) go to the tensor-core prefill kernel, which tiles the
+// queries itself and needs no key split.
+static bool many_rows(int Hq, int Hkv, int T) { return static_cast<long long>(Hq / Hkv) * T > 16; }
+
+static fa_status check_many_rows(int Hq, int Hkv, int num_splits) {
+  const int g = Hq / Hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return FA_ERR_UNSUPPORTED;
+  if (num_splits > 1) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -197,6 +210,16 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
   if (st != FA_OK) return st;
   if (!k || !v || !aligned16(k) || !aligned16(v) || S < 1) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * Hkv * S >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  if (many_rows(Hq, Hkv, T)) {
+    st = check_many_rows(Hq, Hkv, num_splits);
+    if (st != FA_OK) return st;
+    unsigned* err = error_word();
+    if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
+    int rc = launch_prefill_tc(q, k, v, o, lse, B, Hq, Hkv, T, S, d, scale, causal ? 1 : 0,
+                               static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0);
+    if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
+    return static_cast<fa_status>(rc);
+  }
   int n = num_splits;
   if (n == 0) {
     const int sms = sm_count();
@@ -239,6 +262,17 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
   if (page_size != 16) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_pages) * 16 >= (1ll << 31) || static_cast<long long>(max_pages) * 16 >= (1ll << 31))
     return FA_ERR_UNSUPPORTED;
+  if (many_rows(Hq, Hkv, T)) {
+    st = check_many_rows(Hq, Hkv, num_splits);
+    if (st != FA_OK) return st;
+    unsigned* err = error_word();
+    if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
+    int rc = launch_prefill_tc(q, k_pages, v_pages, o, lse, B, Hq, Hkv, T, 0, d, scale, causal ? 1 : 0,
+                               static_cast<cudaStream_t>(stream), err, g_timeout_ns, block_table, seqlens, max_pages,
+                               num_pages);
+    if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
+    return static_cast<fa_status>(rc);
+  }
   int n = num_splits;
   if (n == 0) {
     const int sms = sm_count();

@@ -25,6 +25,7 @@ enum ErrSite : unsigned {
   SITE_DEC_PRODUCER = 5,
   SITE_DEC_CONSUMER = 6,
   SITE_DEC_TABLE = 7,
+  SITE_PF_TABLE = 8,
 };
 
 __device__ __forceinline__ void record_error(unsigned* err, unsigned code, unsigned site) {

@@ -82,6 +82,10 @@ struct PfParams {
   float c;            // scale * log2(e)
   unsigned* err;
   unsigned long long timeout_ns;
+  // paged K/V only: pools [num_pages][16][Hkv][d], block_table [B][max_pages], seqlens [B]
+  const int* block_table;
+  const int* seqlens;
+  int max_pages, num_pages;
 };
 
 struct PfBars {
@@ -102,6 +106,14 @@ struct PfItem {
   int nj[2];  // key tiles tile 0 / 1 needs (0 for a tile past T)
 };
 
+// Keys of sequence b: p.S, or (paged) its seqlens entry clamped to the table's reach.
+// Not carried in PfItem: the contiguous kernel keeps that struct as small as possible.
+template <bool PAGED>
+__device__ __forceinline__ int item_keys(const PfParams& p, int b) {
+  return PAGED ? max(0, min(__ldg(p.seqlens + b), p.max_pages * 16)) : p.S;
+}
+
+template <bool PAGED>
 __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn) {
   PfItem w;
   const int bh_count = p.B * p.Hkv;
@@ -122,14 +134,15 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn) {
   }
   w.b = w.bh / p.Hkv;
   w.kvh = w.bh % p.Hkv;
-  const int shift = p.S - p.T;
+  const int S_b = item_keys<PAGED>(p, w.b);
+  const int shift = S_b - p.T;  // bottom-right: query i sits at key position i + shift
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int first = (2 * qp + t) * p.rows_per_head;
     int kv_end = 0;
     if (first < p.T) {
-      kv_end = p.S;
-      if (p.causal) kv_end = min(p.S, min(first + p.rows_per_head, p.T) - 1 + shift + 1);
+      kv_end = S_b;
+      if (p.causal) kv_end = min(S_b, min(first + p.rows_per_head, p.T) - 1 + shift + 1);
     }
     w.p0[t] = first;
     w.nj[t] = kv_end > 0 ? (kv_end + bn - 1) / bn : 0;
@@ -137,7 +150,7 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn) {
   return w;
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PfParams p) {
@@ -152,7 +165,6 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int shift = p.S - p.T;  // bottom-right alignment: row i sees keys j <= i + shift
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -177,6 +189,8 @@ __global__ void __launch_bounds__(384, 1)
   volatile int* abort_flag = &bars->abort_flag;
   const uint64_t tmo = p.timeout_ns;
 
+  const int shift_all = p.S - p.T;  // contiguous: bottom-right alignment, one shift for every item
+
   auto fail = [&](unsigned site) {
     record_error(p.err, FA_ERR_TIMEOUT, site);
     *abort_flag = 1;
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(384, 1)
       int item_i = 0;
       uint32_t q_loads = 0;  // Q loads issued (q_full phases)
       for (int it = blockIdx.x; it < p.n_items && !*abort_flag; it += gridDim.x, ++item_i) {
-        const PfItem w = pf_item(p, it, C::BN);
+        const PfItem w = pf_item<PAGED>(p, it, C::BN);
         const int nj = max(w.nj[0], w.nj[1]);
         // Q of the previous item stays in smem until its last S has been computed
         if (item_i > 0 && !mbar_wait(&bars->q_empty, (item_i - 1) & 1, tmo, abort_flag)) {
@@ -209,26 +223,75 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, w.p0[t],
                         w.kvh * p.g, w.b);
         ++q_loads;
+        // paged: the 128 keys of tile j are pages 8j .. 8j+7 of the sequence; pages past
+        // its end are not loaded (their K is masked, their V zeroed before use). The
+        // eight table entries of the next tile are fetched while this tile is issued.
+        const int* trow = PAGED ? p.block_table + static_cast<size_t>(w.b) * p.max_pages : nullptr;
+        const int n_pages = (item_keys<PAGED>(p, w.b) + 15) >> 4;
+        int ent[8], ent_next[8];
+        auto fetch = [&](int jt, int (&e)[8]) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int pg = jt * 8 + i;
+            e[i] = (PAGED && jt < nj && pg < n_pages) ? __ldg(trow + pg) : -1;
+          }
+        };
+        if (PAGED) fetch(0, ent_next);
         for (int j = 0; j < nj; ++j, ++g) {
           const int s = g % C::STAGES;
           const uint32_t u = g / C::STAGES;
+          int npg = 8;  // pages of this tile that are loaded
+          if (PAGED) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ent[i] = ent_next[i];
+            fetch(j + 1, ent_next);
+            npg = min(8, n_pages - j * 8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (i < npg && (ent[i] < 0 || ent[i] >= p.num_pages)) {
+                // never dereferenced: the tile still receives the bytes it expects,
+                // from page 0, and the sequence's output is undefined
+                record_error(p.err, FA_ERR_BOUNDS, SITE_PF_TABLE);
+                ent[i] = 0;
+              }
+            }
+          }
+          const uint32_t tile_bytes = PAGED ? static_cast<uint32_t>(npg) * 16 * 128 * C::KCH : C::KV_BYTES;
           if (g >= C::STAGES && !mbar_wait(&bars->k_empty[s], (u - 1) & 1, tmo, abort_flag)) {
             fail(SITE_PF_PRODUCER);
             break;
           }
-          mbar_arrive_expect_tx(&bars->k_full[s], C::KV_BYTES);
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, j * C::BN,
-                        w.bh);
+          mbar_arrive_expect_tx(&bars->k_full[s], tile_bytes);
+          if (PAGED) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i < npg)
+                for (int c = 0; c < C::KCH; ++c)
+                  tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES + i * 16 * 128, &tmK, &bars->k_full[s],
+                              c * 64, w.kvh, ent[i] * 16);
+          } else {
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, j * C::BN,
+                          w.bh);
+          }
           if (g >= C::STAGES && !mbar_wait(&bars->v_empty[s], (u - 1) & 1, tmo, abort_flag)) {
             fail(SITE_PF_PRODUCER);
             mbar_wait(&bars->k_full[s], u & 1, tmo);  // K was issued: let it land
             break;
           }
-          mbar_arrive_expect_tx(&bars->v_full[s], C::KV_BYTES);
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->v_full[s], c * 64, j * C::BN,
-                        w.bh);
+          mbar_arrive_expect_tx(&bars->v_full[s], tile_bytes);
+          if (PAGED) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i < npg)
+                for (int c = 0; c < C::KCH; ++c)
+                  tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES + i * 16 * 128, &tmV, &bars->v_full[s],
+                              c * 64, w.kvh, ent[i] * 16);
+          } else {
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->v_full[s], c * 64, j * C::BN,
+                          w.bh);
+          }
         }
       }
       if (*abort_flag) {
@@ -290,7 +353,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t pph0 = 0, pph1 = 0;   // p_full phase parity of tile 0 / 1
     int item_i = 0;
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++item_i) {
-      const PfItem w = pf_item(p, it, C::BN);
+      const PfItem w = pf_item<PAGED>(p, it, C::BN);
       const int nj0 = w.nj[0], nj1 = w.nj[1];
       const int nj = max(nj0, nj1);
       if (!wwait(&bars->q_full, item_i & 1)) {
@@ -415,8 +478,16 @@ __global__ void __launch_bounds__(384, 1)
     };
     uint32_t cnt = 0;   // key tiles of this query tile done so far, over all items (s_full phases)
     uint32_t ecnt = 0;  // items of this query tile with at least one key tile (pv_done phases)
+    uint32_t gkv = 0;   // K/V ring position at the start of the item (paged V tail zeroing)
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
-      const PfItem w = pf_item(p, it, C::BN);
+      const PfItem w = pf_item<PAGED>(p, it, C::BN);
+      const int S_item = item_keys<PAGED>(p, w.b);  // keys of this item's sequence
+      const int shift = PAGED ? S_item - p.T : shift_all;  // bottom-right: row i sees keys j <= i + shift
+      const int nj_item = max(w.nj[0], w.nj[1]);
+      // paged: V rows past the sequence end in its last key tile hold whatever the pool
+      // (or an earlier tile) left there, possibly NaN, and a zero weight would not cancel
+      // a NaN. The tile that issues the first PV on that key tile zeroes them first.
+      const bool v_tail_owner = PAGED && nj_item > 0 && nj_item * C::BN > S_item && t == (w.nj[0] == nj_item ? 0 : 1);
       // selects, not a runtime index into w (which would put w in local memory)
       const int my_nj = t ? w.nj[1] : w.nj[0];
       const int my_p0 = t ? w.p0[1] : w.p0[0];
@@ -442,9 +513,9 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
 
         const int key0 = j * C::BN;
-        const bool need_mask = (key0 + C::BN > p.S) || (p.causal && key0 + C::BN - 1 > my_p0 + shift);
+        const bool need_mask = (key0 + C::BN > S_item) || (p.causal && key0 + C::BN - 1 > my_p0 + shift);
         if (need_mask) {
-          const int lim = (p.causal ? min(p.S - 1, vis_last) : p.S - 1) - key0;
+          const int lim = (p.causal ? min(S_item - 1, vis_last) : S_item - 1) - key0;
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (i > lim) s[i] = -INFINITY;
@@ -509,10 +580,29 @@ __global__ void __launch_bounds__(384, 1)
             tmem_st32(tO + cc * 32 + 32, o1);
           }
         }
+        if (v_tail_owner && j + 1 == nj_item) {
+          // zero V rows S_item - key0 .. 127 of this key tile once its copy has landed,
+          // then make the generic stores visible to the tensor core's reads
+          const uint32_t x = gkv + j;
+          if (!wwait(&bars->v_full[x % C::STAGES], (x / C::STAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t* vt = sV + (x % C::STAGES) * C::KV_BYTES;
+          const int r0 = S_item - key0;
+          for (int idx = r; idx < (C::BN - r0) * C::KCH * 8; idx += 128) {
+            const int row = r0 + idx / (C::KCH * 8);
+            const int rem = idx % (C::KCH * 8);
+            *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::CHUNK_BYTES + row * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+        }
         tmem_st_wait();  // P (and O) stores complete before the MMA may read them
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
       }
+      gkv += nj_item;
 
       // ---- epilogue: O / l -> bf16, lse = ln2 * (m + log2 l)
       if (ok && my_nj > 0) {
@@ -574,11 +664,26 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn get_encode_tiled();  // defined in api.cu
 int device_sm_count();              // defined in api.cu
 
+template <int D, bool PAGED>
+static int launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfParams& p, int grid,
+                     cudaStream_t stream) {
+  auto kfn = prefill_tc_kernel<D, PAGED>;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::SMEM) != cudaSuccess)
+    return FA_ERR_CUDA;
+  kfn<<<grid, PfCfg<D>::THREADS, PfCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Contiguous K/V ([B][Hkv][S][d]) when block_table is null; otherwise `k`/`v` are
+// pools [num_pages][16][Hkv][d] shared through block_table [B][max_pages], with
+// seqlens [B] keys per sequence (S is then unused).
 int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                       int T, int S, int d, float scale, int causal, cudaStream_t stream, unsigned* err,
-                      unsigned long long timeout_ns) {
+                      unsigned long long timeout_ns, const int* block_table, const int* seqlens, int max_pages,
+                      int num_pages) {
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return FA_ERR_CUDA;
+  const bool paged = block_table != nullptr;
   const int g = Hq / Hkv;
   const int rows_per_head = 128 / g;
   CUtensorMap tq, tk, tv;
@@ -593,9 +698,22 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, floa
       return FA_ERR_CUDA;
   }
   for (int w = 0; w < 2; ++w) {
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)B * Hkv};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint64_t dims[3];
+    cuuint64_t strides[2];
+    cuuint32_t box[3];
+    if (!paged) {
+      // 128 keys of one (batch, KV head) per box
+      dims[0] = d; dims[1] = S; dims[2] = static_cast<cuuint64_t>(B) * Hkv;
+      strides[0] = static_cast<cuuint64_t>(d) * 2;
+      strides[1] = static_cast<cuuint64_t>(S) * d * 2;
+      box[0] = 64; box[1] = 128; box[2] = 1;
+    } else {
+      // one 16-token page of one KV head per box
+      dims[0] = d; dims[1] = Hkv; dims[2] = static_cast<cuuint64_t>(num_pages) * 16;
+      strides[0] = static_cast<cuuint64_t>(d) * 2;
+      strides[1] = static_cast<cuuint64_t>(Hkv) * d * 2;
+      box[0] = 64; box[1] = 1; box[2] = 16;
+    }
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(w == 0 ? &tk : &tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w == 0 ? k : v), dims,
             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -609,7 +727,7 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, floa
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.T = T;
-  p.S = S;
+  p.S = paged ? max_pages * 16 : S;
   p.g = g;
   p.rows_per_head = rows_per_head;
   p.n_qtiles = (T + rows_per_head - 1) / rows_per_head;
@@ -618,6 +736,10 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, floa
   p.c = scale * kLog2e;
   p.err = err;
   p.timeout_ns = timeout_ns;
+  p.block_table = block_table;
+  p.seqlens = seqlens;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
   const long long items = static_cast<long long>(p.n_pairs) * B * Hkv;
   if (items > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   p.n_items = static_cast<int>(items);
@@ -625,18 +747,8 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, floa
   const int sms = device_sm_count();
   if (sms <= 0) return FA_ERR_CUDA;
   const int grid = items < sms ? static_cast<int>(items) : sms;
-  if (d == 128) {
-    auto kfn = prefill_tc_kernel<128>;
-    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<128>::SMEM) != cudaSuccess)
-      return FA_ERR_CUDA;
-    kfn<<<grid, PfCfg<128>::THREADS, PfCfg<128>::SMEM, stream>>>(tq, tk, tv, p);
-  } else {
-    auto kfn = prefill_tc_kernel<64>;
-    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<64>::SMEM) != cudaSuccess)
-      return FA_ERR_CUDA;
-    kfn<<<grid, PfCfg<64>::THREADS, PfCfg<64>::SMEM, stream>>>(tq, tk, tv, p);
-  }
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (d == 128) return paged ? launch_pf<128, true>(tq, tk, tv, p, grid, stream) : launch_pf<128, false>(tq, tk, tv, p, grid, stream);
+  return paged ? launch_pf<64, true>(tq, tk, tv, p, grid, stream) : launch_pf<64, false>(tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace fa

@@ -56,6 +56,13 @@ PAGED_DECODE = Workload("paged_decode_b64_hq64_hkv8_s8192_d128_p16", 4, 64, 64, 
 
 WORKLOADS = {w.name: w for w in (SMOKE, PREFILL_MHA, CAUSAL_GQA, SPLITKV_DECODE, PAGED_DECODE)}
 
+# Beyond the five: chunked prefill over the paged cache. Each of 8 sequences
+# appends 512 new tokens to a cache of CHUNKED_SEQLENS[b] tokens (the new ones
+# included), 16-token pages scattered by the seeded permutation.
+CHUNKED_PREFILL = Workload("chunked_prefill_paged_b8_hq32_hkv8_t512_s8192_d128_p16", 5, 8, 32, 8, 512, 8192, 128,
+                           True, page_size=16, note="512 new tokens per sequence over a paged cache of up to 8192")
+CHUNKED_SEQLENS = (8192, 7000, 6144, 5000, 4096, 3000, 2048, 1024)
+
 
 def _gen(seed: int, device="cpu") -> torch.Generator:
     g = torch.Generator(device=device)
@@ -98,6 +105,14 @@ def paged_kv(B, Hkv, S, d, page_size, index: int, dtype=torch.bfloat16, device="
 
 def decode_q(B, Hq, T, d, index: int, dtype=torch.bfloat16, device="cpu"):
     return randn((B, Hq, T, d), 1000 + index, dtype, device)
+
+
+def chunked_prefill_problem(w: Workload = CHUNKED_PREFILL, device="cpu"):
+    """q [B][Hq][T][d], the paged pools, block table and seqlens of the chunked-prefill workload."""
+    k_pages, v_pages, table, _ = paged_kv(w.B, w.Hkv, w.S, w.d, w.page_size, w.index, device=device)
+    q = decode_q(w.B, w.Hq, w.T, w.d, w.index, device=device)
+    seqlens = torch.tensor(CHUNKED_SEQLENS[: w.B], dtype=torch.int32, device=device)
+    return q, k_pages, v_pages, table, seqlens
 
 
 def sample_rows(B, Hq, T, n: int, seed: int, tile: int = 128):

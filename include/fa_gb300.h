@@ -120,7 +120,12 @@ FA_API size_t fa_decode_workspace_bytes(int B, int Hq, int T, int d, int num_spl
  * many splits for decode".)
  *   q [B][Hq][T][d] bf16; k, v [B][Hkv][S][d] bf16; o [B][Hq][T][d] bf16 out;
  *   lse [B][Hq][T] fp32 out (may be NULL).
- *   d in {64, 128}; (Hq / Hkv) * T <= 16.
+ *   d in {64, 128}.
+ *   With more than 16 query rows per KV head ((Hq / Hkv) * T > 16: a chunked
+ *   prefill or a multi-token step) the call runs the tensor-core prefill
+ *   kernel, which tiles the queries itself: num_splits must then be 0 or 1,
+ *   Hq / Hkv one of 1, 2, 4, 8, 16 (else FA_ERR_UNSUPPORTED), and no
+ *   workspace is used. The result is the same attention.
  *   num_splits: 0 = fa_num_splits_heuristic(B, Hkv, S, SM count); else 1..1024.
  *   workspace: device scratch of at least fa_decode_workspace_bytes(...)
  *   bytes, 256-byte aligned (may be NULL when the split count is 1).
@@ -139,7 +144,8 @@ FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, 
  * The partials go to a fixed 4 MiB array inside the library's device image
  * (every device that loads the library holds one until the process exits);
  * the call allocates nothing.
- *   Arguments and results as fa_decode_splitkv.
+ *   Arguments and results as fa_decode_splitkv, except that (Hq / Hkv) * T
+ *   must be <= 16 (FA_ERR_UNSUPPORTED otherwise).
  *   Returns FA_ERR_UNSUPPORTED when the partials would need more than 4 MiB,
  *   i.e. fa_decode_workspace_bytes(B, Hq, T, d, splits) > 4194304.
  *   The first call on a device looks up the array's device address (with
@@ -175,9 +181,15 @@ FA_API fa_status fa_lse_merge(const float* o_part, const float* lse_part, void* 
  *   block_table [B][max_pages] int32 (device)
  *   seqlens     [B] int32 (device): keys of each sequence, each in [0, max_pages*page_size]
  *   o, lse      as fa_decode_splitkv
- *   page_size == 16; d in {64, 128}; (Hq / Hkv) * T <= 16.
+ *   page_size == 16; d in {64, 128}.
  *   Each sequence's keys are split into num_splits ranges (0 = heuristic on
  *   max_pages*page_size); workspace as fa_decode_splitkv.
+ *   With (Hq / Hkv) * T > 16 (chunked prefill over the cache: T new tokens at
+ *   positions seqlens[b] - T .. seqlens[b] - 1 under the bottom-right mask)
+ *   the tensor-core prefill kernel gathers each 128-key tile from eight pages;
+ *   the same rules as in fa_decode_splitkv apply (num_splits 0 or 1, no
+ *   workspace). Pool rows past a sequence's end are never used, whatever
+ *   they hold.
  *   A table entry outside [0, num_pages) is not dereferenced: the kernel
  *   records FA_ERR_BOUNDS (read it with fa_get_last_device_error) and that
  *   sequence's output is undefined.

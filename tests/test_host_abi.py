@@ -78,8 +78,14 @@ def test_fwd_rejects_bad_arguments(L):
 
 
 def test_decode_rejects_bad_arguments(L):
-    # group 8 x T 3 = 24 stacked rows > 16
-    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 1, 3, 100, 128, 0.1, 1, 1, None, 0, None) == _lib.FA_ERR_UNSUPPORTED
+    # more than 16 stacked rows (group 8 x T 3 = 24) run on the prefill kernel, which
+    # takes no key split and only groups of 1, 2, 4, 8, 16: both refused before any launch
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 1, 3, 100, 128, 0.1, 1, 2, None, 0, None) == _lib.FA_ERR_UNSUPPORTED
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 6, 2, 9, 100, 128, 0.1, 1, 1, None, 0, None) == _lib.FA_ERR_UNSUPPORTED
+    args = [P, P, P, P, P, P, None, 2, 8, 1, 3, 4, 16, 8, 128, 0.1, 1, 4, None, 0, None]
+    assert L.fa_decode_paged(*args) == _lib.FA_ERR_UNSUPPORTED
+    # the static-scratch entry keeps the 16-row limit
+    assert L.fa_decode_splitkv_static(P, P, P, P, None, 1, 8, 1, 3, 100, 128, 0.1, 1, 1, None) == _lib.FA_ERR_UNSUPPORTED
     # a split count above one needs a large enough, 256-byte aligned workspace
     assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 2, 1, 100, 128, 0.1, 1, 4, None, 0, None) == _lib.FA_ERR_INVALID_ARG
     need = L.fa_decode_workspace_bytes(1, 8, 1, 128, 4)

@@ -22,6 +22,28 @@ def attention_flops(B: int, Hq: int, T: int, S: int, d: int, causal: bool) -> fl
     return f / 2.0 if causal else f
 
 
+def visible_pairs(T: int, S: int, causal: bool) -> int:
+    """(query, key) pairs the mask leaves visible for T queries over S keys.
+
+    Bottom-right alignment: query i (0-based) sits at key position i + S - T and
+    sees keys 0 .. min(S - 1, i + S - T); rows past the start see none.
+    """
+    if not causal:
+        return T * S
+    total = 0
+    lo = S - T + 1  # keys row 0 sees (may be <= 0)
+    # rows with a positive count form an arithmetic run capped at S
+    for i in range(T):
+        total += max(0, min(S, lo + i))
+    return total
+
+
+def chunked_attention_flops(Hq: int, T: int, seqlens, d: int, causal: bool = True) -> float:
+    """4*d FLOP per visible (query, key) pair and query head, summed over sequences:
+    T new queries per sequence over its seqlens[b] keys, bottom-right aligned."""
+    return 4.0 * Hq * d * sum(visible_pairs(T, int(S), causal) for S in seqlens)
+
+
 def standard_attention_bytes(N: int, d: int, e: int = 2) -> float:
     """Three-kernel attention of one head: read Q, K; write+read S; write+read P; read V; write O."""
     return e * (2 * N * d + 4 * N * N + 2 * N * d)

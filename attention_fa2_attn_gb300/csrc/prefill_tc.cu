@@ -54,7 +54,11 @@ struct PfCfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + slack to align the base to 1024
+  // paged: the batch's sequences ranked by key count (longest first), for the item order
+  static constexpr int MAX_RANKED = 512;
+  static constexpr int OFF_ORDER = OFF_BAR + BAR_BYTES;
+  static constexpr int SMEM = OFF_ORDER + 1024;                     // + slack to align the base to 1024
+  static constexpr int SMEM_PAGED = OFF_ORDER + MAX_RANKED * 4 + 1024;
   static constexpr int TMEM_COLS = 512;
   static constexpr int TILE_COLS = 256;   // TMEM columns per query tile: S/P then O
   static constexpr int O_OFF = 128;       // O region inside a tile's columns
@@ -114,11 +118,26 @@ __device__ __forceinline__ int item_keys(const PfParams& p, int b) {
 }
 
 template <bool PAGED>
-__device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn) {
+__device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn, const int* order) {
   PfItem w;
   const int bh_count = p.B * p.Hkv;
   int qp;
-  if (p.causal) {
+  if (PAGED) {
+    // Sequences of a paged batch differ in length, so item weights differ by
+    // sequence: items go longest sequence first (order[] ranks them when the batch
+    // has at most MAX_RANKED sequences), within it heaviest query-tile pair first,
+    // dealt to the CTAs in the same snake order as below.
+    const int G = gridDim.x;
+    const int round = it / G;
+    const int x = it - round * G;
+    const int sorted = ((round & 1) && (round + 1) * G <= p.n_items) ? round * G + (G - 1 - x) : it;
+    const int per_b = p.Hkv * p.n_pairs;
+    const int rank = sorted / per_b;
+    const int within = sorted - rank * per_b;
+    const int b = order ? order[rank] : rank;
+    qp = p.n_pairs - 1 - within / p.Hkv;
+    w.bh = b * p.Hkv + within % p.Hkv;
+  } else if (p.causal) {
     // items sorted heaviest first, dealt to the CTAs in snake order (rounds of
     // gridDim.x alternate direction) so that every CTA's total is close to the mean;
     // the last, partial round keeps the forward direction
@@ -183,6 +202,21 @@ __global__ void __launch_bounds__(384, 1)
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+  // paged: rank the sequences by key count, longest first (ties by index)
+  int* order_smem = reinterpret_cast<int*>(smem + C::OFF_ORDER);
+  const int* order = nullptr;
+  if (PAGED && p.B <= C::MAX_RANKED) {
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+      const int sb = item_keys<PAGED>(p, b);
+      int rank = 0;
+      for (int b2 = 0; b2 < p.B; ++b2) {
+        const int s2 = item_keys<PAGED>(p, b2);
+        rank += (s2 > sb || (s2 == sb && b2 < b)) ? 1 : 0;
+      }
+      order_smem[rank] = b;
+    }
+    order = order_smem;
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
@@ -202,74 +236,79 @@ __global__ void __launch_bounds__(384, 1)
     warpgroup_reg_dealloc<C::AUX_REGS>();
   if (warp == C::PRODUCER_WARP) {
     // ======================= TMA producer =======================
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+    // Contiguous K/V: one lane does everything. Paged K/V: a key tile is 16 page
+    // boxes per operand, so the whole warp runs the loop (its waits are uniform:
+    // every lane polls the same barrier in one instruction), lanes 0-7 hold the
+    // tile's table entries, and one box per lane is issued after lane 0 has armed
+    // the barrier.
+    if (PAGED || lane == 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
       uint32_t g = 0;  // key tiles loaded so far, over all items (ring position)
       int item_i = 0;
       uint32_t q_loads = 0;  // Q loads issued (q_full phases)
       for (int it = blockIdx.x; it < p.n_items && !*abort_flag; it += gridDim.x, ++item_i) {
-        const PfItem w = pf_item<PAGED>(p, it, C::BN);
+        const PfItem w = pf_item<PAGED>(p, it, C::BN, order);
         const int nj = max(w.nj[0], w.nj[1]);
         // Q of the previous item stays in smem until its last S has been computed
         if (item_i > 0 && !mbar_wait(&bars->q_empty, (item_i - 1) & 1, tmo, abort_flag)) {
           fail(SITE_PF_PRODUCER);
           break;
         }
-        mbar_arrive_expect_tx(&bars->q_full, C::QT * C::Q_BYTES);
-        for (int t = 0; t < 2; ++t)
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, w.p0[t],
-                        w.kvh * p.g, w.b);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->q_full, C::QT * C::Q_BYTES);
+          for (int t = 0; t < 2; ++t)
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_4d(sQ + t * C::Q_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, w.p0[t],
+                          w.kvh * p.g, w.b);
+        }
         ++q_loads;
         // paged: the 128 keys of tile j are pages 8j .. 8j+7 of the sequence; pages past
-        // its end are not loaded (their K is masked, their V zeroed before use). The
-        // eight table entries of the next tile are fetched while this tile is issued.
+        // its end are not loaded (their K is masked, their V zeroed before use). Lane
+        // i < 8 holds the entry of page 8j + i; the next tile's are fetched while this
+        // tile is issued.
         const int* trow = PAGED ? p.block_table + static_cast<size_t>(w.b) * p.max_pages : nullptr;
         const int n_pages = (item_keys<PAGED>(p, w.b) + 15) >> 4;
-        int ent[8], ent_next[8];
-        auto fetch = [&](int jt, int (&e)[8]) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int pg = jt * 8 + i;
-            e[i] = (PAGED && jt < nj && pg < n_pages) ? __ldg(trow + pg) : -1;
-          }
+        auto fetch = [&](int jt) -> int {
+          const int pg = jt * 8 + lane;
+          return (PAGED && lane < 8 && jt < nj && pg < n_pages) ? __ldg(trow + pg) : -1;
         };
-        if (PAGED) fetch(0, ent_next);
+        int ent_next = PAGED ? fetch(0) : -1;
         for (int j = 0; j < nj; ++j, ++g) {
           const int s = g % C::STAGES;
           const uint32_t u = g / C::STAGES;
           int npg = 8;  // pages of this tile that are loaded
+          int ent = -1;
           if (PAGED) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ent[i] = ent_next[i];
-            fetch(j + 1, ent_next);
+            ent = ent_next;
+            ent_next = fetch(j + 1);
             npg = min(8, n_pages - j * 8);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (i < npg && (ent[i] < 0 || ent[i] >= p.num_pages)) {
-                // never dereferenced: the tile still receives the bytes it expects,
-                // from page 0, and the sequence's output is undefined
-                record_error(p.err, FA_ERR_BOUNDS, SITE_PF_TABLE);
-                ent[i] = 0;
-              }
+            if (lane < npg && (ent < 0 || ent >= p.num_pages)) {
+              // never dereferenced: the tile still receives the bytes it expects,
+              // from page 0, and the sequence's output is undefined
+              record_error(p.err, FA_ERR_BOUNDS, SITE_PF_TABLE);
+              ent = 0;
             }
           }
           const uint32_t tile_bytes = PAGED ? static_cast<uint32_t>(npg) * 16 * 128 * C::KCH : C::KV_BYTES;
+          // paged: lane L issues the box of page L / KCH, d-chunk L % KCH
+          const int pi = lane / C::KCH, pc = lane % C::KCH;
+          const int pe = PAGED ? __shfl_sync(0xffffffffu, ent, pi & 7) : 0;
           if (g >= C::STAGES && !mbar_wait(&bars->k_empty[s], (u - 1) & 1, tmo, abort_flag)) {
             fail(SITE_PF_PRODUCER);
             break;
           }
-          mbar_arrive_expect_tx(&bars->k_full[s], tile_bytes);
           if (PAGED) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i < npg)
-                for (int c = 0; c < C::KCH; ++c)
-                  tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES + i * 16 * 128, &tmK, &bars->k_full[s],
-                              c * 64, w.kvh, ent[i] * 16);
+            if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[s], tile_bytes);
+            __syncwarp();
+            if (pi < npg)
+              tma_load_3d(sK + s * C::KV_BYTES + pc * C::CHUNK_BYTES + pi * 16 * 128, &tmK, &bars->k_full[s],
+                          pc * 64, w.kvh, pe * 16);
           } else {
+            mbar_arrive_expect_tx(&bars->k_full[s], tile_bytes);
             for (int c = 0; c < C::KCH; ++c)
               tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, j * C::BN,
                           w.bh);
@@ -279,15 +318,14 @@ __global__ void __launch_bounds__(384, 1)
             mbar_wait(&bars->k_full[s], u & 1, tmo);  // K was issued: let it land
             break;
           }
-          mbar_arrive_expect_tx(&bars->v_full[s], tile_bytes);
           if (PAGED) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i < npg)
-                for (int c = 0; c < C::KCH; ++c)
-                  tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES + i * 16 * 128, &tmV, &bars->v_full[s],
-                              c * 64, w.kvh, ent[i] * 16);
+            if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[s], tile_bytes);
+            __syncwarp();
+            if (pi < npg)
+              tma_load_3d(sV + s * C::KV_BYTES + pc * C::CHUNK_BYTES + pi * 16 * 128, &tmV, &bars->v_full[s],
+                          pc * 64, w.kvh, pe * 16);
           } else {
+            mbar_arrive_expect_tx(&bars->v_full[s], tile_bytes);
             for (int c = 0; c < C::KCH; ++c)
               tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->v_full[s], c * 64, j * C::BN,
                           w.bh);
@@ -353,7 +391,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t pph0 = 0, pph1 = 0;   // p_full phase parity of tile 0 / 1
     int item_i = 0;
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++item_i) {
-      const PfItem w = pf_item<PAGED>(p, it, C::BN);
+      const PfItem w = pf_item<PAGED>(p, it, C::BN, order);
       const int nj0 = w.nj[0], nj1 = w.nj[1];
       const int nj = max(nj0, nj1);
       if (!wwait(&bars->q_full, item_i & 1)) {
@@ -480,7 +518,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t ecnt = 0;  // items of this query tile with at least one key tile (pv_done phases)
     uint32_t gkv = 0;   // K/V ring position at the start of the item (paged V tail zeroing)
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
-      const PfItem w = pf_item<PAGED>(p, it, C::BN);
+      const PfItem w = pf_item<PAGED>(p, it, C::BN, order);
       const int S_item = item_keys<PAGED>(p, w.b);  // keys of this item's sequence
       const int shift = PAGED ? S_item - p.T : shift_all;  // bottom-right: row i sees keys j <= i + shift
       const int nj_item = max(w.nj[0], w.nj[1]);
@@ -668,9 +706,10 @@ template <int D, bool PAGED>
 static int launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfParams& p, int grid,
                      cudaStream_t stream) {
   auto kfn = prefill_tc_kernel<D, PAGED>;
-  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::SMEM) != cudaSuccess)
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  kfn<<<grid, PfCfg<D>::THREADS, PfCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
+  kfn<<<grid, PfCfg<D>::THREADS, PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

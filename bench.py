@@ -348,6 +348,32 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
                    "bytes_per_step": byt, "num_splits": 1,
                    "traffic": load_traffic().get("decode_kernel_paged")}
     del q, kp, vp, table, sl, o, lse
+
+    # chunked prefill over the paged cache (the prefill kernel through fa_decode_paged)
+    w = fi.CHUNKED_PREFILL
+    max_pages = w.S // w.page_size
+    P = w.B * max_pages
+    q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)
+    kp = rnd((P, w.page_size, w.Hkv, w.d), 2000 + w.index)
+    vp = rnd((P, w.page_size, w.Hkv, w.d), 3000 + w.index)
+    cpu_gen = torch.Generator().manual_seed(4000 + w.index)
+    table = torch.randperm(P, generator=cpu_gen).view(w.B, max_pages).to(torch.int32).to(dev)
+    seqlens = fi.CHUNKED_SEQLENS[: w.B]
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.T, device=dev)
+    step = lambda: fa.fa_decode_paged(q, kp, vp, table, sl, causal=True, num_splits=0, scale=w.scale,  # noqa: E731
+                                      out=o, lse=lse)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(torch, step, steps, stream)
+    tf = cm.chunked_attention_flops(w.Hq, w.T, seqlens, w.d, True) / (ms * 1e-3) / 1e12
+    out[w.name] = {"metric": "attn fwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                   "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 1,
+                   "flops": "4*d per visible (query, key) pair under the bottom-right mask",
+                   "seqlens": list(seqlens)}
+    del q, kp, vp, table, sl, o, lse
     torch.cuda.empty_cache()
     return out
 

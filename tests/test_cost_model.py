@@ -70,3 +70,14 @@ def test_decode_bytes_for_the_workloads():
     # paged decode: 64 sequences * 8 heads * 8192 tokens * 128 * 2 B * (K, V)
     assert cm.decode_kv_bytes(64, 8, 8192, 128) == 2147483648
     assert cm.decode_bytes(64, 64, 8, 1, 8192, 128, page_size=16) > cm.decode_kv_bytes(64, 8, 8192, 128)
+
+
+def test_visible_pairs_brute_force():
+    """The closed-loop count equals enumerating the mask (key j visible iff j <= i + S - T)."""
+    for T, S in ((1, 7), (5, 5), (9, 4), (512, 8192), (33, 20), (3, 0)):
+        brute = sum(1 for i in range(T) for j in range(S) if j <= i + S - T)
+        assert cm.visible_pairs(T, S, True) == brute
+        assert cm.visible_pairs(T, S, False) == T * S
+    # square causal: N(N+1)/2, the exact count behind the "halved" convention
+    assert cm.visible_pairs(4096, 4096, True) == 4096 * 4097 // 2
+    assert cm.chunked_attention_flops(2, 3, [3, 5], 8) == 4.0 * 2 * 8 * (6 + 12)

@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     fa_get_last_device_error,
     fa_lse_merge,
     fa_num_splits_heuristic,
+    fa_num_splits_prefill,
     fa_selftest_wait_timeout,
     fa_set_wait_timeout_ns,
 )

@@ -36,6 +36,7 @@ SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_fwd_f32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_num_splits_heuristic": (_I, [_I, _I, _I, _I]),
+    "fa_num_splits_prefill": (_I, [_I, _I, _I, _I, _I, _I]),
     "fa_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "fa_decode_splitkv_static": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),

@@ -70,11 +70,18 @@ def fa_decode_workspace_bytes(B: int, Hq: int, T: int, d: int, num_splits: int) 
     return int(lib().fa_decode_workspace_bytes(B, Hq, T, d, num_splits))
 
 
-def _resolve_splits(num_splits: int, B: int, Hq: int, Hkv: int, T: int, S: int, device) -> int:
-    if num_splits or (Hq // Hkv) * T > 16:
-        # more than 16 stacked query rows run on the prefill kernel, without a key split
+def fa_num_splits_prefill(B: int, Hq: int, Hkv: int, T: int, S: int, num_sms: int) -> int:
+    return int(lib().fa_num_splits_prefill(B, Hq, Hkv, T, S, num_sms))
+
+
+def _resolve_splits(num_splits: int, B: int, Hq: int, Hkv: int, T: int, S: int, device, paged: bool = False) -> int:
+    if num_splits:
         return int(num_splits)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
+    if (Hq // Hkv) * T > 16:
+        # more than 16 stacked query rows run on the prefill kernel; it splits the
+        # keys only when its query tiles do not fill the GPU (contiguous K/V)
+        return 1 if paged else fa_num_splits_prefill(B, Hq, Hkv, T, S, sms)
     return fa_num_splits_heuristic(B, Hkv, S, sms)
 
 
@@ -152,7 +159,7 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = Tr
     P, page_size, Hkv, _ = k_pages.shape
     max_pages = block_table.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    n = _resolve_splits(num_splits, B, Hq, Hkv, T, max_pages * page_size, q.device)
+    n = _resolve_splits(num_splits, B, Hq, Hkv, T, max_pages * page_size, q.device, paged=True)
     ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
     o = torch.empty_like(q) if out is None else out
     if lse is None:
@@ -187,6 +194,7 @@ __all__ = [
     "fa_fwd",
     "fa_fwd_f32",
     "fa_num_splits_heuristic",
+    "fa_num_splits_prefill",
     "fa_decode_workspace_bytes",
     "fa_decode_splitkv",
     "fa_decode_splitkv_static",

@@ -18,7 +18,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                       int T, int S, int d, float scale, int causal, cudaStream_t stream, unsigned* err,
                       unsigned long long timeout_ns, const int* block_table, const int* seqlens, int max_pages,
-                      int num_pages);
+                      int num_pages, int num_splits, float* o_part, float* lse_part);
 int launch_prefill_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq, int Hkv,
                        int T, int S, int d, float scale, int causal, cudaStream_t stream);
 int launch_decode(const void* q, const void* k, const void* v, const int* block_table, const int* seqlens, void* o,
@@ -140,6 +140,21 @@ int fa_num_splits_heuristic(int B, int Hkv, int S, int num_sms) {
   return n < 1 ? 1 : static_cast<int>(n);
 }
 
+int fa_num_splits_prefill(int B, int Hq, int Hkv, int T, int S, int num_sms) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || num_sms <= 0 || Hq % Hkv != 0) return 1;
+  const long long g = Hq / Hkv;
+  if (g > 128) return 1;
+  const long long rows_per_tile = 128 / g;                    // query positions per 128-row tile
+  const long long tiles = (T + rows_per_tile - 1) / rows_per_tile;
+  const long long units = (tiles + 1) / 2 * B * Hkv;          // query-tile pairs: the unsplit work items
+  if (units >= num_sms) return 1;
+  long long n = num_sms / units;                              // fill at most one wave
+  const long long cap = (S + 511) / 512;                      // at least four 128-key tiles per range
+  if (n > cap) n = cap;
+  if (n > 64) n = 64;
+  return n < 1 ? 1 : static_cast<int>(n);
+}
+
 size_t fa_decode_workspace_bytes(int B, int Hq, int T, int d, int num_splits) {
   if (num_splits <= 1 || B <= 0 || Hq <= 0 || T <= 0 || d <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * T;
@@ -161,7 +176,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   unsigned* err = error_word();
   if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
   int rc = launch_prefill_tc(q, k, v, o, lse, B, Hq, Hkv, Tq, Skv, d, scale, causal ? 1 : 0,
-                             static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0);
+                             static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0, 1, nullptr,
+                             nullptr);
   if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
   return static_cast<fa_status>(rc);
 }
@@ -193,14 +209,23 @@ static fa_status check_decode_common(const void* q, const void* o, int B, int Hq
 
 // More than 16 stacked query rows per KV head (g * T > 16: chunked prefill or a
 // multi-token decode step) go to the tensor-core prefill kernel, which tiles the
-// queries itself and needs no key split.
+// queries itself; a key split is then only for shapes with too few query tiles to
+// fill the GPU (contiguous K/V).
 static bool many_rows(int Hq, int Hkv, int T) { return static_cast<long long>(Hq / Hkv) * T > 16; }
 
-static fa_status check_many_rows(int Hq, int Hkv, int num_splits) {
+static fa_status check_many_rows(int Hq, int Hkv, int num_splits, bool paged) {
   const int g = Hq / Hkv;
   if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return FA_ERR_UNSUPPORTED;
-  if (num_splits > 1) return FA_ERR_UNSUPPORTED;
+  if (paged && num_splits > 1) return FA_ERR_UNSUPPORTED;
   return FA_OK;
+}
+
+// Splits that fit in ws_bytes (partials plus lse, as fa_decode_workspace_bytes lays them out).
+static int splits_that_fit(int B, int Hq, int T, int d, int want, const void* workspace, size_t ws_bytes) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return 1;
+  int n = want;
+  while (n > 1 && fa_decode_workspace_bytes(B, Hq, T, d, n) > ws_bytes) --n;
+  return n;
 }
 
 fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
@@ -211,12 +236,33 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
   if (!k || !v || !aligned16(k) || !aligned16(v) || S < 1) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * Hkv * S >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
   if (many_rows(Hq, Hkv, T)) {
-    st = check_many_rows(Hq, Hkv, num_splits);
+    st = check_many_rows(Hq, Hkv, num_splits, false);
     if (st != FA_OK) return st;
+    int n = num_splits;
+    if (n == 0) {
+      // heuristic, limited to what the given workspace holds (none: no split)
+      const int sms = sm_count();
+      if (!sms) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
+      n = splits_that_fit(B, Hq, T, d, fa_num_splits_prefill(B, Hq, Hkv, T, S, sms), workspace, ws_bytes);
+    } else if (n > 1) {
+      if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+      if (ws_bytes < fa_decode_workspace_bytes(B, Hq, T, d, n)) return FA_ERR_INVALID_ARG;
+    }
     unsigned* err = error_word();
     if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
+    float* o_part = nullptr;
+    float* lse_part = nullptr;
+    const size_t rows = static_cast<size_t>(B) * Hq * T;
+    if (n > 1) {
+      o_part = static_cast<float*>(workspace);
+      const size_t obytes = ((static_cast<size_t>(n) * rows * d * 4 + 255) / 256) * 256;
+      lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + obytes);
+    }
     int rc = launch_prefill_tc(q, k, v, o, lse, B, Hq, Hkv, T, S, d, scale, causal ? 1 : 0,
-                               static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0);
+                               static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0, n, o_part,
+                               lse_part);
+    if (rc == FA_OK && n > 1)
+      rc = launch_lse_merge(o_part, lse_part, o, lse, n, static_cast<int>(rows), d, static_cast<cudaStream_t>(stream));
     if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
     return static_cast<fa_status>(rc);
   }
@@ -263,13 +309,13 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
   if (static_cast<long long>(num_pages) * 16 >= (1ll << 31) || static_cast<long long>(max_pages) * 16 >= (1ll << 31))
     return FA_ERR_UNSUPPORTED;
   if (many_rows(Hq, Hkv, T)) {
-    st = check_many_rows(Hq, Hkv, num_splits);
+    st = check_many_rows(Hq, Hkv, num_splits, true);
     if (st != FA_OK) return st;
     unsigned* err = error_word();
     if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
     int rc = launch_prefill_tc(q, k_pages, v_pages, o, lse, B, Hq, Hkv, T, 0, d, scale, causal ? 1 : 0,
                                static_cast<cudaStream_t>(stream), err, g_timeout_ns, block_table, seqlens, max_pages,
-                               num_pages);
+                               num_pages, 1, nullptr, nullptr);
     if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
     return static_cast<fa_status>(rc);
   }

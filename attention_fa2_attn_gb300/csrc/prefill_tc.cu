@@ -90,6 +90,11 @@ struct PfParams {
   const int* block_table;
   const int* seqlens;
   int max_pages, num_pages;
+  // key split only: num_splits ranges of split_tiles 128-key tiles each; partials
+  // o_part [num_splits][B*Hq*T][D] fp32 (normalised) and lse_part [num_splits][B*Hq*T]
+  int num_splits, split_tiles;
+  float* o_part;
+  float* lse_part;
 };
 
 struct PfBars {
@@ -117,12 +122,23 @@ __device__ __forceinline__ int item_keys(const PfParams& p, int b) {
   return PAGED ? max(0, min(__ldg(p.seqlens + b), p.max_pages * 16)) : p.S;
 }
 
-template <bool PAGED>
+// Key split: item `it` covers key tiles split_j0 .. of range it % num_splits.
+template <bool SPLIT>
+__device__ __forceinline__ int split_j0(const PfParams& p, int it) {
+  return SPLIT ? (it % p.num_splits) * p.split_tiles : 0;
+}
+
+template <bool PAGED, bool SPLIT = false>
 __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn, const int* order) {
   PfItem w;
   const int bh_count = p.B * p.Hkv;
   int qp;
-  if (PAGED) {
+  if (SPLIT) {
+    // low-occupancy shapes: (query-tile pair, key range) units, head-major
+    const int base = it / p.num_splits;
+    w.bh = base / p.n_pairs;
+    qp = base % p.n_pairs;
+  } else if (PAGED) {
     // Sequences of a paged batch differ in length, so item weights differ by
     // sequence: items go longest sequence first (order[] ranks them when the batch
     // has at most MAX_RANKED sequences), within it heaviest query-tile pair first,
@@ -155,6 +171,7 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn, con
   w.kvh = w.bh % p.Hkv;
   const int S_b = item_keys<PAGED>(p, w.b);
   const int shift = S_b - p.T;  // bottom-right: query i sits at key position i + shift
+  const int lo = split_j0<SPLIT>(p, it) * bn;  // first key of this item's range
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int first = (2 * qp + t) * p.rows_per_head;
@@ -163,13 +180,14 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn, con
       kv_end = S_b;
       if (p.causal) kv_end = min(S_b, min(first + p.rows_per_head, p.T) - 1 + shift + 1);
     }
+    if (SPLIT) kv_end = min(kv_end, lo + p.split_tiles * bn);
     w.p0[t] = first;
-    w.nj[t] = kv_end > 0 ? (kv_end + bn - 1) / bn : 0;
+    w.nj[t] = kv_end > lo ? (kv_end - lo + bn - 1) / bn : 0;
   }
   return w;
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PfParams p) {
@@ -251,7 +269,7 @@ __global__ void __launch_bounds__(384, 1)
       int item_i = 0;
       uint32_t q_loads = 0;  // Q loads issued (q_full phases)
       for (int it = blockIdx.x; it < p.n_items && !*abort_flag; it += gridDim.x, ++item_i) {
-        const PfItem w = pf_item<PAGED>(p, it, C::BN, order);
+        const PfItem w = pf_item<PAGED, SPLIT>(p, it, C::BN, order);
         const int nj = max(w.nj[0], w.nj[1]);
         // Q of the previous item stays in smem until its last S has been computed
         if (item_i > 0 && !mbar_wait(&bars->q_empty, (item_i - 1) & 1, tmo, abort_flag)) {
@@ -270,6 +288,7 @@ __global__ void __launch_bounds__(384, 1)
         // its end are not loaded (their K is masked, their V zeroed before use). Lane
         // i < 8 holds the entry of page 8j + i; the next tile's are fetched while this
         // tile is issued.
+        const int j0 = split_j0<SPLIT>(p, it);  // first key tile of the item's range
         const int* trow = PAGED ? p.block_table + static_cast<size_t>(w.b) * p.max_pages : nullptr;
         const int n_pages = (item_keys<PAGED>(p, w.b) + 15) >> 4;
         auto fetch = [&](int jt) -> int {
@@ -310,7 +329,7 @@ __global__ void __launch_bounds__(384, 1)
           } else {
             mbar_arrive_expect_tx(&bars->k_full[s], tile_bytes);
             for (int c = 0; c < C::KCH; ++c)
-              tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, j * C::BN,
+              tma_load_3d(sK + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->k_full[s], c * 64, (j0 + j) * C::BN,
                           w.bh);
           }
           if (g >= C::STAGES && !mbar_wait(&bars->v_empty[s], (u - 1) & 1, tmo, abort_flag)) {
@@ -327,7 +346,7 @@ __global__ void __launch_bounds__(384, 1)
           } else {
             mbar_arrive_expect_tx(&bars->v_full[s], tile_bytes);
             for (int c = 0; c < C::KCH; ++c)
-              tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->v_full[s], c * 64, j * C::BN,
+              tma_load_3d(sV + s * C::KV_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->v_full[s], c * 64, (j0 + j) * C::BN,
                           w.bh);
           }
         }
@@ -391,7 +410,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t pph0 = 0, pph1 = 0;   // p_full phase parity of tile 0 / 1
     int item_i = 0;
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++item_i) {
-      const PfItem w = pf_item<PAGED>(p, it, C::BN, order);
+      const PfItem w = pf_item<PAGED, SPLIT>(p, it, C::BN, order);
       const int nj0 = w.nj[0], nj1 = w.nj[1];
       const int nj = max(nj0, nj1);
       if (!wwait(&bars->q_full, item_i & 1)) {
@@ -518,7 +537,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t ecnt = 0;  // items of this query tile with at least one key tile (pv_done phases)
     uint32_t gkv = 0;   // K/V ring position at the start of the item (paged V tail zeroing)
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
-      const PfItem w = pf_item<PAGED>(p, it, C::BN, order);
+      const PfItem w = pf_item<PAGED, SPLIT>(p, it, C::BN, order);
       const int S_item = item_keys<PAGED>(p, w.b);  // keys of this item's sequence
       const int shift = PAGED ? S_item - p.T : shift_all;  // bottom-right: row i sees keys j <= i + shift
       const int nj_item = max(w.nj[0], w.nj[1]);
@@ -550,7 +569,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(raw[i >> 5][i & 31]);
 
-        const int key0 = j * C::BN;
+        const int key0 = (split_j0<SPLIT>(p, it) + j) * C::BN;
         const bool need_mask = (key0 + C::BN > S_item) || (p.causal && key0 + C::BN - 1 > my_p0 + shift);
         if (need_mask) {
           const int lim = (p.causal ? min(S_item - 1, vis_last) : S_item - 1) - key0;
@@ -664,7 +683,17 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = 0u;
           }
-          if (row_valid) {
+          if (SPLIT) {
+            // the range's normalised partial, fp32, for the LSE merge
+            if (row_valid) {
+              float* prow = p.o_part + (static_cast<size_t>(it % p.num_splits) * p.B * p.Hq * p.T + row_index) * D;
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(prow + cc * 32 + 4 * q) =
+                    make_float4(__uint_as_float(o[4 * q + 0]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+            }
+          } else if (row_valid) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 v;
@@ -676,7 +705,12 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         }
-        if (row_valid && p.lse) p.lse[row_index] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (SPLIT) {
+          if (row_valid) p.lse_part[static_cast<size_t>(it % p.num_splits) * p.B * p.Hq * p.T + row_index] = lse_v;
+        } else if (row_valid && p.lse) {
+          p.lse[row_index] = lse_v;
+        }
       }
       // O_t has been read out (the loads above completed); these threads arrive on
       // p_full for the next item only after this, so the MMA warp's wait for that P
@@ -702,10 +736,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn get_encode_tiled();  // defined in api.cu
 int device_sm_count();              // defined in api.cu
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool SPLIT = false>
 static int launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfParams& p, int grid,
                      cudaStream_t stream) {
-  auto kfn = prefill_tc_kernel<D, PAGED>;
+  auto kfn = prefill_tc_kernel<D, PAGED, SPLIT>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
@@ -715,11 +749,14 @@ static int launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 // Contiguous K/V ([B][Hkv][S][d]) when block_table is null; otherwise `k`/`v` are
 // pools [num_pages][16][Hkv][d] shared through block_table [B][max_pages], with
-// seqlens [B] keys per sequence (S is then unused).
+// seqlens [B] keys per sequence (S is then unused). num_splits > 1 (contiguous
+// only): the keys are cut into num_splits ranges of whole 128-key tiles and the
+// kernel writes normalised fp32 partials to o_part / lse_part (layout of
+// fa_decode_workspace_bytes) instead of o / lse; the caller merges them.
 int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                       int T, int S, int d, float scale, int causal, cudaStream_t stream, unsigned* err,
                       unsigned long long timeout_ns, const int* block_table, const int* seqlens, int max_pages,
-                      int num_pages) {
+                      int num_pages, int num_splits, float* o_part, float* lse_part) {
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return FA_ERR_CUDA;
   const bool paged = block_table != nullptr;
@@ -779,15 +816,26 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, void* o, floa
   p.seqlens = seqlens;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
-  const long long items = static_cast<long long>(p.n_pairs) * B * Hkv;
+  const bool split = num_splits > 1 && !paged;
+  p.num_splits = split ? num_splits : 1;
+  // ranges of whole key tiles: no tile is shared by two ranges
+  p.split_tiles = split ? ((S + 127) / 128 + num_splits - 1) / num_splits : 0;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  const long long items = static_cast<long long>(p.n_pairs) * B * Hkv * p.num_splits;
   if (items > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   p.n_items = static_cast<int>(items);
   // persistent: one CTA per SM, each takes items blockIdx.x, blockIdx.x + grid, ...
   const int sms = device_sm_count();
   if (sms <= 0) return FA_ERR_CUDA;
   const int grid = items < sms ? static_cast<int>(items) : sms;
-  if (d == 128) return paged ? launch_pf<128, true>(tq, tk, tv, p, grid, stream) : launch_pf<128, false>(tq, tk, tv, p, grid, stream);
-  return paged ? launch_pf<64, true>(tq, tk, tv, p, grid, stream) : launch_pf<64, false>(tq, tk, tv, p, grid, stream);
+  if (d == 128) {
+    if (paged) return launch_pf<128, true>(tq, tk, tv, p, grid, stream);
+    return split ? launch_pf<128, false, true>(tq, tk, tv, p, grid, stream)
+                 : launch_pf<128, false>(tq, tk, tv, p, grid, stream);
+  }
+  if (paged) return launch_pf<64, true>(tq, tk, tv, p, grid, stream);
+  return split ? launch_pf<64, false, true>(tq, tk, tv, p, grid, stream) : launch_pf<64, false>(tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace fa

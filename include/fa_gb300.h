@@ -106,6 +106,18 @@ FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, floa
 FA_API int fa_num_splits_heuristic(int B, int Hkv, int S, int num_sms);
 
 /*
+ * fa_num_splits_prefill -- key ranges for a call with more than 16 query rows
+ * per KV head (a prefill-shaped problem) whose query tiles alone do not fill
+ * the GPU, e.g. one head of a long sequence. The same one-wave rule as the
+ * decode heuristic ("How many splits for decode"), counted in the prefill
+ * kernel's work items: units = ceil(ceil(T / (128 / g)) / 2) * B * Hkv pairs
+ * of 128-row query tiles (g = Hq / Hkv). Returns 1 when units >= num_sms,
+ * else max(1, min(num_sms / units, ceil(S / 512), 64)).
+ * Pure host arithmetic. Returns 1 for invalid arguments.
+ */
+FA_API int fa_num_splits_prefill(int B, int Hq, int Hkv, int T, int S, int num_sms);
+
+/*
  * fa_decode_workspace_bytes -- bytes of `workspace` a split decode needs:
  * FP32 partial outputs [num_splits][B*Hq*T][d] followed (256-byte aligned) by
  * FP32 partial lse [num_splits][B*Hq*T]. 0 when num_splits <= 1.
@@ -122,10 +134,13 @@ FA_API size_t fa_decode_workspace_bytes(int B, int Hq, int T, int d, int num_spl
  *   lse [B][Hq][T] fp32 out (may be NULL).
  *   d in {64, 128}.
  *   With more than 16 query rows per KV head ((Hq / Hkv) * T > 16: a chunked
- *   prefill or a multi-token step) the call runs the tensor-core prefill
- *   kernel, which tiles the queries itself: num_splits must then be 0 or 1,
- *   Hq / Hkv one of 1, 2, 4, 8, 16 (else FA_ERR_UNSUPPORTED), and no
- *   workspace is used. The result is the same attention.
+ *   prefill, a multi-token step, or a whole prefill) the call runs the
+ *   tensor-core prefill kernel, which tiles the queries itself; Hq / Hkv must
+ *   be one of 1, 2, 4, 8, 16 (else FA_ERR_UNSUPPORTED). num_splits > 1 cuts
+ *   the keys into that many ranges of whole 128-key tiles for shapes whose
+ *   query tiles do not fill the GPU, with the workspace and merge as above;
+ *   num_splits == 0 takes fa_num_splits_prefill, lowered to what `workspace`
+ *   holds (no workspace: no split). The result is the same attention.
  *   num_splits: 0 = fa_num_splits_heuristic(B, Hkv, S, SM count); else 1..1024.
  *   workspace: device scratch of at least fa_decode_workspace_bytes(...)
  *   bytes, 256-byte aligned (may be NULL when the split count is 1).
@@ -187,9 +202,9 @@ FA_API fa_status fa_lse_merge(const float* o_part, const float* lse_part, void* 
  *   With (Hq / Hkv) * T > 16 (chunked prefill over the cache: T new tokens at
  *   positions seqlens[b] - T .. seqlens[b] - 1 under the bottom-right mask)
  *   the tensor-core prefill kernel gathers each 128-key tile from eight pages;
- *   the same rules as in fa_decode_splitkv apply (num_splits 0 or 1, no
- *   workspace). Pool rows past a sequence's end are never used, whatever
- *   they hold.
+ *   num_splits must then be 0 or 1 (no key split, no workspace) and Hq / Hkv
+ *   one of 1, 2, 4, 8, 16. Pool rows past a sequence's end are never used,
+ *   whatever they hold.
  *   A table entry outside [0, num_pages) is not dereferenced: the kernel
  *   records FA_ERR_BOUNDS (read it with fa_get_last_device_error) and that
  *   sequence's output is undefined.

@@ -103,18 +103,21 @@ def test_paged_chunked_equals_contiguous_bit_exact():
         assert torch.equal(o1, o2) and torch.equal(l1, l2), causal
 
 
-def test_contiguous_many_rows_and_split_refusal():
-    """fa_decode_splitkv with 256 stacked rows runs the prefill kernel; a key split
-    is refused there rather than silently ignored."""
+def test_contiguous_many_rows():
+    """fa_decode_splitkv with 256 stacked rows runs the prefill kernel, unsplit or
+    with its keys cut into ranges; a key split over the paged cache is refused
+    rather than silently ignored."""
     fa = _fa()
     B, Hq, Hkv, T, S, d = 1, 8, 2, 64, 3000, 128
     q, k, v = fi.qkv(B, Hq, Hkv, T, S, d, 99)
     scale = 1.0 / math.sqrt(d)
     o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, True)
-    o, l = fa.fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, num_splits=0, scale=scale)
-    compare(o, l, o_ref, l_ref, what="contiguous many rows")
+    for n in (1, 3):
+        o, l = fa.fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, num_splits=n, scale=scale)
+        compare(o, l, o_ref, l_ref, what=f"contiguous many rows, {n} ranges")
+    qp, kp, vp, table, sl = _paged_problem(1, 8, 2, 64, 128, [3000], 188, 99)
     with pytest.raises(fa.FAError):
-        fa.fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, num_splits=3, scale=scale)
+        fa.fa_decode_paged(qp.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), sl.to(DEV), num_splits=3)
 
 
 def test_chunked_bad_table_entry_is_reported():

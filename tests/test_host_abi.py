@@ -52,6 +52,19 @@ def test_split_heuristic_page_example(L):
     assert L.fa_num_splits_heuristic(0, 8, 100, 152) == 1
 
 
+def test_prefill_split_heuristic(L):
+    # one head of 8192 positions, d any: 64 query tiles -> 32 pairs; 152 SMs -> 4 ranges
+    assert L.fa_num_splits_prefill(1, 1, 1, 8192, 8192, 152) == 4
+    # one head of 4096: 16 pairs -> 9 ranges (ceil(4096 / 512) = 8 caps it)
+    assert L.fa_num_splits_prefill(1, 1, 1, 4096, 4096, 152) == 8
+    # the prefill workload already fills the GPU: 4 x 16 heads x 16 pairs
+    assert L.fa_num_splits_prefill(4, 16, 16, 4096, 4096, 152) == 1
+    # GQA: 8 query heads per KV head stack 16 positions per 128-row tile
+    assert L.fa_num_splits_prefill(1, 8, 1, 1024, 65536, 152) == 4  # 64 tiles -> 32 pairs
+    assert L.fa_num_splits_prefill(1, 6, 4, 100, 100, 152) == 1  # Hq not a multiple of Hkv
+    assert L.fa_num_splits_prefill(1, 1, 1, 128, 100000, 152) == 64  # one pair: capped at 64
+
+
 def test_workspace_bytes(L):
     assert L.fa_decode_workspace_bytes(1, 32, 1, 128, 1) == 0
     n, rows, d = 16, 32, 128
@@ -78,9 +91,9 @@ def test_fwd_rejects_bad_arguments(L):
 
 
 def test_decode_rejects_bad_arguments(L):
-    # more than 16 stacked rows (group 8 x T 3 = 24) run on the prefill kernel, which
-    # takes no key split and only groups of 1, 2, 4, 8, 16: both refused before any launch
-    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 1, 3, 100, 128, 0.1, 1, 2, None, 0, None) == _lib.FA_ERR_UNSUPPORTED
+    # more than 16 stacked rows (group 8 x T 3 = 24) run on the prefill kernel: its key
+    # split needs the workspace like decode's, and it takes only groups of 1, 2, 4, 8, 16
+    assert L.fa_decode_splitkv(P, P, P, P, None, 1, 8, 1, 3, 100, 128, 0.1, 1, 2, None, 0, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_decode_splitkv(P, P, P, P, None, 1, 6, 2, 9, 100, 128, 0.1, 1, 1, None, 0, None) == _lib.FA_ERR_UNSUPPORTED
     args = [P, P, P, P, P, P, None, 2, 8, 1, 3, 4, 16, 8, 128, 0.1, 1, 4, None, 0, None]
     assert L.fa_decode_paged(*args) == _lib.FA_ERR_UNSUPPORTED

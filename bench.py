@@ -374,6 +374,36 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
                    "flops": "4*d per visible (query, key) pair under the bottom-right mask",
                    "seqlens": list(seqlens)}
     del q, kp, vp, table, sl, o, lse
+
+    # the prefill workload's one-head sweep: too few query tiles for 152 SMs, so the
+    # keys are split (fa_num_splits_prefill) and the partials merged
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sweep = {}
+    for N, d in fi.PREFILL_MHA.sweep:
+        q = rnd((1, 1, N, d), 1000 + fi.PREFILL_MHA.index)
+        k = rnd((1, 1, N, d), 2000 + fi.PREFILL_MHA.index)
+        v = rnd((1, 1, N, d), 3000 + fi.PREFILL_MHA.index)
+        o = torch.empty_like(q)
+        lse = torch.empty(1, 1, N, device=dev)
+        n = fa.fa_num_splits_prefill(1, 1, 1, N, N, sms)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(1, 1, N, d, n), dtype=torch.uint8, device=dev)
+        flops = cm.attention_flops(1, 1, N, N, d, False)
+        res = {}
+        for label, step in (
+            ("unsplit", lambda: fa.fa_fwd(q, k, v, causal=False, out=o, lse=lse)),
+            ("split", lambda: fa.fa_decode_splitkv(q, k, v, causal=False, num_splits=n, workspace=ws, out=o, lse=lse)),
+        ):
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            ms = time_steps(torch, step, steps, stream)
+            res[label] = {"TFLOP/s": flops / (ms * 1e-3) / 1e12, "ms_per_step": ms}
+        res["num_splits"] = n
+        res["launches_per_step_split"] = 2
+        sweep[f"N{N}_d{d}"] = res
+        del q, k, v, o, lse, ws
+    out["prefill_one_head_sweep_b1_h1"] = {"metric": "attn fwd TFLOP/s", "unit": "TFLOP/s", "non_causal": True,
+                                          "shapes": sweep}
     torch.cuda.empty_cache()
     return out
 

@@ -13,11 +13,13 @@ forms, or an independent brute force. No function is "parity unpinned".
 
 from .attention import (  # noqa: F401
     NEG_INF,
+    attention_backward,
     attention_online,
     attention_online_normalized,
     attention_partials,
     attention_rows,
     attention_three_pass,
+    backward_rowsum,
     causal_mask,
     decode_paged,
     kv_head_of,

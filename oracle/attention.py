@@ -421,3 +421,77 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, page_size: int, scal
         ob, lb = attention_three_pass(_as64(q[b : b + 1]), kb, vb, scale, causal)
         o[b], lse[b] = ob[0], lb[0]
     return o, lse
+
+
+# --------------------------------------------------------------------------- #
+# Backward: gradients of O with respect to Q, K and V
+# --------------------------------------------------------------------------- #
+def _bwd_probs(x, lse, vis):
+    """P = exp(S - LSE) from the saved log-sum-exp ([CHAIN] "What the backward pass
+    saves"); masked entries and rows with no visible key (lse = -inf) give 0."""
+    p = np.zeros_like(x)
+    live = np.isfinite(lse)
+    if live.any():
+        p[live] = np.where(vis[live], np.exp(x[live] - lse[live, None]), 0.0)
+    return p
+
+
+def _softmax_grad(p, dp, dsum):
+    """dS = P * (dP - D): the softmax Jacobian applied to dP, with D = rowsum(dO * O)."""
+    return p * (dp - dsum[:, None])
+
+
+def _score_grads(ds, q, k, scale):
+    """Through S = scale * Q K^T: dQ = scale * dS K, dK = scale * dS^T Q."""
+    return scale * (ds @ k), scale * (ds.T @ q)
+
+
+def attention_backward(q, k, v, do, scale: float, causal: bool = False, o=None, lse=None):
+    """Gradients of O = softmax(scale * Q K^T) V for an upstream gradient dO.
+
+    [CHAIN] "What the backward pass saves": the forward keeps Q, K, V, O and one
+    log-sum-exp per query row; the backward rebuilds each probability as
+    P = exp(S - LSE) with S = scale * Q K^T, and the softmax gradient needs the
+    one extra vector D = rowsum(dO * O), formed once before the main loop. The
+    rest is the chain rule through O = P V and P = softmax(S), written out per
+    (batch, query head):
+        dV  = P^T dO                 (O = P V)
+        dP  = dO V^T
+        dS  = P * (dP - D)           (softmax Jacobian: dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik),
+                                      and sum_k P_ik dP_ik = dO_i . O_i = D_i)
+        dQ  = scale * dS K           (S = scale * Q K^T)
+        dK  = scale * dS^T Q
+    A KV head's dK and dV sum over the query heads of its group (GQA: head h
+    reads KV head h // g). Masked scores have P = 0; a row with no visible key
+    contributes nothing.
+    o, lse: the saved forward outputs; when omitted they come from the
+    three-pass forward. q, do [B][Hq][T][d]; k, v [B][Hkv][S][d].
+    Returns (dq, dk, dv) in fp64 with the shapes of q, k, v.
+    """
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    B, Hq, Hkv, T, S, d = _check_shapes(q, k, v)
+    if o is None or lse is None:
+        o, lse = attention_three_pass(q, k, v, scale, causal)
+    o, lse = _as64(o), _as64(lse)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    vis = causal_mask(T, S, causal)
+    dsum_all = backward_rowsum(do, o)  # D, once before the main loop
+    for b in range(B):
+        for h in range(Hq):
+            hk = kv_head_of(h, Hq, Hkv)
+            x = scale * (q[b, h] @ k[b, hk].T)  # S
+            p = _bwd_probs(x, lse[b, h], vis)
+            dp = do[b, h] @ v[b, hk].T
+            ds = _softmax_grad(p, dp, dsum_all[b, h])
+            dv[b, hk] += p.T @ do[b, h]
+            dqh, dkh = _score_grads(ds, q[b, h], k[b, hk], scale)
+            dq[b, h] = dqh
+            dk[b, hk] += dkh
+    return dq, dk, dv
+
+
+def backward_rowsum(do, o):
+    """D = rowsum(dO * O), one value per query row ([CHAIN] "What the backward pass saves")."""
+    return (_as64(do) * _as64(o)).sum(axis=-1)

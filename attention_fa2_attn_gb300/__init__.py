@@ -7,6 +7,8 @@ same names, ``costmodel`` the FLOP and byte accounting used for rooflines.
 
 from .api import (  # noqa: F401
     FAError,
+    fa_bwd,
+    fa_bwd_workspace_bytes,
     fa_decode_paged,
     fa_decode_splitkv,
     fa_decode_splitkv_static,

@@ -62,6 +62,34 @@ def fa_fwd_f32(q, k, v, causal: bool = False, scale: float | None = None):
     return o, lse
 
 
+def fa_bwd_workspace_bytes(B: int, Hq: int, T: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, Hq, T))
+
+
+def fa_bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None, workspace=None,
+           dq=None, dk=None, dv=None):
+    """Backward: q, o, d_o [B][Hq][T][d], k, v [B][Hkv][S][d] bf16, lse [B][Hq][T] fp32
+    (the forward's) -> (dq, dk, dv) bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (d_o, "d_o")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    B, Hq, T, d = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = fa_bwd_workspace_bytes(B, Hq, T)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
+                      Hkv, T, S, d, scale, int(causal), _ptr(workspace), workspace.numel(), _stream(q))
+    check(st, "fa_bwd")
+    return dq, dk, dv
+
+
 def fa_num_splits_heuristic(B: int, Hkv: int, S: int, num_sms: int) -> int:
     return int(lib().fa_num_splits_heuristic(B, Hkv, S, num_sms))
 
@@ -193,6 +221,8 @@ __all__ = [
     "FAError",
     "fa_fwd",
     "fa_fwd_f32",
+    "fa_bwd",
+    "fa_bwd_workspace_bytes",
     "fa_num_splits_heuristic",
     "fa_num_splits_prefill",
     "fa_decode_workspace_bytes",

@@ -27,6 +27,9 @@ int launch_decode(const void* q, const void* k, const void* v, const int* block_
                   unsigned long long timeout_ns);
 int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows, int d,
                      cudaStream_t stream);
+int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
+                    void* dq, void* dk, void* dv, float* dsum, int B, int Hq, int Hkv, int T, int S, int d,
+                    float scale, int causal, cudaStream_t stream, unsigned* err, unsigned long long timeout_ns);
 
 // The device-side error word (code | site << 8). Kernels receive its device
 // address as a parameter.
@@ -178,6 +181,36 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   int rc = launch_prefill_tc(q, k, v, o, lse, B, Hq, Hkv, Tq, Skv, d, scale, causal ? 1 : 0,
                              static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0, 1, nullptr,
                              nullptr);
+  if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
+  return static_cast<fa_status>(rc);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int T) {
+  if (B <= 0 || Hq <= 0 || T <= 0) return 0;
+  return static_cast<size_t>(B) * Hq * T * 4;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
+                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq, int Skv, int d, float scale, int causal,
+                 void* workspace, size_t ws_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Skv < 1 || Hq % Hkv != 0 || !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u) || ws_bytes < fa_bwd_workspace_bytes(B, Hq, Tq))
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const int g = Hq / Hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq * Tq >= (1ll << 31) || static_cast<long long>(B) * Hkv * Skv >= (1ll << 31) ||
+      static_cast<long long>(B) * Hkv > 65535)
+    return FA_ERR_UNSUPPORTED;
+  unsigned* err = error_word();
+  if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
+  int rc = launch_backward(q, k, v, o, lse, d_o, dq, dk, dv, static_cast<float*>(workspace), B, Hq, Hkv, Tq, Skv, d,
+                           scale, causal ? 1 : 0, static_cast<cudaStream_t>(stream), err, g_timeout_ns);
   if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
   return static_cast<fa_status>(rc);
 }

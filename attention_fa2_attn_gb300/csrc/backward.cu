@@ -1,0 +1,665 @@
+// backward.cu -- attention backward: dQ, dK, dV for O = softmax(scale * Q K^T) V.
+//
+// What it computes ("Attention kernel chains", "What the backward pass saves"):
+// the forward keeps Q, K, V, O and one log-sum-exp per query row; the backward
+// rebuilds each probability tile on chip as P = exp(S - LSE) and needs one more
+// vector, D = rowsum(dO * O), formed once before the main loops. With
+// S = scale * Q K^T, the chain rule through O = P V and P = softmax(S) gives
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q,
+// a KV head's dK, dV summing over the query heads of its group; masked scores
+// (bottom-right causal mask) have P = 0.
+//
+// How (GB300-specific): three launches.
+//   * bwd_rowsum_kernel: D, one warp per query row (HBM-bound, tiny).
+//   * bwd_dq_kernel: one 128-row query tile per CTA (a GQA group's heads stacked
+//     as rows, as in the forward) looping over 128-key tiles. tcgen05 MMAs put
+//     S = Q K^T and dP = dO V^T in TMEM; four warps (one row per thread) form
+//     dS = P * (dP - D) in bf16 over S's columns; dQ += dS K takes dS straight
+//     from TMEM as the A operand.
+//   * bwd_dkdv_kernel: one 128-key tile per CTA looping over the query tiles.
+//     S^T = K Q^T and dP^T = V dO^T in TMEM (rows = keys); the warps write P^T and
+//     dS^T in bf16 over them; dV += P^T dO and dK += dS^T Q read them from TMEM,
+//     with dO and Q as MN-major operands from shared memory. dK and dV
+//     accumulate in TMEM over all query tiles and all heads of the group.
+// Computing dQ in its own kernel (recomputing S and dP there) keeps every
+// accumulator in TMEM and needs no atomics. Each step runs the two MMA groups
+// and the elementwise pass in turn.
+#include "common.cuh"
+
+namespace fa {
+
+// ---------------------------------------------------------------------------
+// D = rowsum(dO * O): one warp per row
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) bwd_rowsum_kernel(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ d_o,
+                                                         float* __restrict__ dsum, long long rows, int d) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(o + row * d);
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(d_o + row * d);
+  float acc = 0.f;
+  for (int c = lane; c < d / 2; c += 32) {
+    const float2 x = __bfloat1622float2(a[c]);
+    const float2 y = __bfloat1622float2(b[c]);
+    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) dsum[row] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// Shared configuration
+// ---------------------------------------------------------------------------
+template <int D>
+struct BwCfg {
+  static constexpr int BM = 128;                 // rows of a tile (TMEM lanes)
+  static constexpr int BN = 128;                 // columns of S (keys, or queries for S^T)
+  static constexpr int KCH = D / 64;             // 128-byte chunks along d
+  static constexpr int CHUNK_BYTES = 128 * 128;  // one 128-row x 128-byte swizzled chunk
+  static constexpr int TILE_BYTES = 128 * D * 2; // one 128-row tile of Q, dO, K or V
+  static constexpr int STAGES = 2;
+  // smem: two fixed tiles (Q and dO, or K and V), then a ring of STAGES tile pairs
+  static constexpr int OFF_FIX = 0;
+  static constexpr int OFF_RING = 2 * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + STAGES * 2 * TILE_BYTES;
+  static constexpr int OFF_VEC = OFF_BAR + 256;  // dK/dV: per-step LSE and D of the query columns
+  static constexpr int SMEM = OFF_VEC + 2 * 2 * BM * 4 + 1024;
+  static constexpr int THREADS = 192;            // warps 0-3 elementwise, 4 producer, 5 MMA
+  static constexpr int PRODUCER_WARP = 4;
+  static constexpr int MMA_WARP = 5;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int COL_S = 0;                // S (or S^T): fp32; P / dS (bf16) later over it
+  static constexpr int COL_DP = 128;             // dP (or dP^T)
+  static constexpr int COL_ACC = 256;            // dQ, or dV then dK
+};
+
+struct BwParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* lse;   // [B][Hq][T], natural log
+  const float* dsum;  // D = rowsum(dO * O), [B][Hq][T]
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int B, Hq, Hkv, T, S;
+  int g, rows_per_head, n_qtiles, n_ktiles;
+  int causal;
+  float scale;
+  float c;  // scale * log2(e)
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+struct BwBars {
+  uint64_t fix_full;      // the fixed tile pair landed
+  uint64_t ring_full[2];  // a ring stage (tile pair) landed
+  uint64_t ring_empty[2]; // a ring stage's last reader finished
+  uint64_t s_full;        // S and dP (or S^T and dP^T) of this step are in TMEM
+  uint64_t e_done;        // the elementwise warps have written this step's operands
+  uint64_t acc_done;      // the last accumulation finished
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Row r of a stacked 128-row query tile qt: head h_local = r / rows_per_head of
+// the group, position qt * rows_per_head + r % rows_per_head.
+__device__ __forceinline__ void bw_row(const BwParams& p, int qt, int r, int& h_local, int& pos) {
+  h_local = r / p.rows_per_head;
+  pos = qt * p.rows_per_head + (r % p.rows_per_head);
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one stacked query tile per CTA, looping over key tiles
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwParams p) {
+  using C = BwCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_FIX;
+  uint8_t* sDO = sQ + C::TILE_BYTES;
+  uint8_t* sRing = smem + C::OFF_RING;  // stage s: K at s * 2 * TILE, V right after
+  BwBars* bars = reinterpret_cast<BwBars*>(smem + C::OFF_BAR);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qt = blockIdx.x;
+  const int bkv = blockIdx.y;
+  const int b = bkv / p.Hkv;
+  const int kvh = bkv % p.Hkv;
+  const int shift = p.S - p.T;
+  // key tiles this query tile needs: causal stops at the last row's diagonal
+  int kv_end = p.S;
+  if (p.causal) kv_end = min(p.S, min((qt + 1) * p.rows_per_head, p.T) - 1 + shift + 1);
+  const int nj = kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->fix_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->ring_full[s], 1);
+      mbar_init(&bars->ring_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->e_done, 128);
+    mbar_init(&bars->acc_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort_flag = &bars->abort_flag;
+  const uint64_t tmo = p.timeout_ns;
+  auto fail = [&](unsigned site) {
+    record_error(p.err, FA_ERR_TIMEOUT, site);
+    *abort_flag = 1;
+  };
+
+  if (warp == C::PRODUCER_WARP) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->fix_full, 2 * C::TILE_BYTES);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_4d(sQ + c * C::CHUNK_BYTES, &tmQ, &bars->fix_full, c * 64, qt * p.rows_per_head, kvh * p.g, b);
+        tma_load_4d(sDO + c * C::CHUNK_BYTES, &tmDO, &bars->fix_full, c * 64, qt * p.rows_per_head, kvh * p.g, b);
+      }
+      int issued = 0;
+      for (int j = 0; j < nj; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&bars->ring_empty[s], ((j >> 1) - 1) & 1, tmo, abort_flag)) {
+          fail(SITE_BW_PRODUCER);
+          break;
+        }
+        uint8_t* st = sRing + s * 2 * C::TILE_BYTES;
+        mbar_arrive_expect_tx(&bars->ring_full[s], 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_3d(st + c * C::CHUNK_BYTES, &tmK, &bars->ring_full[s], c * 64, j * C::BN, bkv);
+          tma_load_3d(st + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->ring_full[s], c * 64, j * C::BN, bkv);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // copies in flight must land before the CTA exits
+        mbar_wait(&bars->fix_full, 0, tmo);
+        for (int x = max(0, issued - 2); x < issued; ++x) mbar_wait(&bars->ring_full[x & 1], (x >> 1) & 1, tmo);
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    const bool leader = elect_one();
+    constexpr uint32_t idesc_ss = idesc_bf16_f32(128, C::BN, 0, 0);  // A, B K-major
+    constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, 0, 1);      // A from TMEM, B MN-major
+    const uint64_t dQd = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dDOd = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+    const uint64_t dRingK = smem_desc_sw128(smem_u32(sRing), 16, 1024);                   // K as the B of S
+    const uint64_t dRingKmn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);     // K as the B of dQ
+    const uint64_t dRingV = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), 16, 1024);   // V as the B of dP
+    bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
+    for (int j = 0; ok && j < nj; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait(&bars->ring_full[s], (j >> 1) & 1, tmo, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t so = static_cast<uint64_t>((s * 2 * C::TILE_BYTES) >> 4);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + C::COL_S, dQd + off, dRingK + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + C::COL_DP, dDOd + off, dRingV + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&bars->s_full);
+      }
+      // dS (bf16, over S's first 64 columns) -> dQ += dS K
+      if (!mbar_wait(&bars->e_done, j & 1, tmo, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + kk * 8, dRingKmn + so + static_cast<uint64_t>((kk * 2048) >> 4),
+                    idesc_ts, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars->ring_empty[s]);
+      }
+    }
+    if (!ok && leader) fail(SITE_BW_MMA);
+    if (leader) tc_commit(&bars->acc_done);
+    mbar_wait(&bars->acc_done, 0, tmo);
+  } else {
+    // ---- elementwise warps: one query row per thread (TMEM lane)
+    const int r = threadIdx.x;  // 0..127
+    int h_local, pos;
+    bw_row(p, qt, r, h_local, pos);
+    const bool row_valid = pos < p.T;
+    const int h = kvh * p.g + h_local;
+    const size_t row_index = (static_cast<size_t>(b) * p.Hq + h) * p.T + (row_valid ? pos : 0);
+    // P = 2^(S*c - lse*log2e); rows past T and rows with no visible key get P = 0
+    const float lse_row = row_valid ? __ldg(p.lse + row_index) : -INFINITY;
+    const float lse2 = lse_row == -INFINITY ? INFINITY : lse_row * kLog2e;
+    const float d_row = row_valid ? __ldg(p.dsum + row_index) : 0.f;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::COL_S;
+    const uint32_t tDP = tmem + lane_base + C::COL_DP;
+    const float c = p.c;
+    bool ok = true;
+    for (int j = 0; j < nj; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, tmo, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int key0 = j * C::BN;
+      // last visible key of this row (bottom-right causal), relative to key0
+      const int lim = (p.causal ? min(p.S - 1, pos + shift) : p.S - 1) - key0;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + cc * 32, sr);
+        tmem_ld32(tDP + cc * 32, dr);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float ds2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = cc * 32 + 2 * i + e;
+            const float pv = col > lim ? 0.f : ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), c, -lse2));
+            ds2[e] = pv * (__uint_as_float(dr[2 * i + e]) - d_row);
+          }
+          pk[i] = pack_bf16x2(ds2[0], ds2[1]);
+        }
+        tmem_st16(tS + cc * 16, pk);  // keys 32cc .. +31 -> columns 16cc .. +15 (already read)
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->e_done);
+    }
+    if (!ok) fail(SITE_BW_ELEM);
+    // ---- epilogue: dQ = scale * (dS K) -> bf16
+    if (ok && nj > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_done, 0, tmo, abort_flag));
+      tc_fence_after();
+    }
+    if (ok) {
+      // every lane loads (tcgen05.ld is warp-collective); rows past T store nothing
+      __nv_bfloat16* drow = p.dq + row_index * D;
+      const float sc = p.scale;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t a[32];
+        if (nj > 0) {
+          tmem_ld32(tmem + lane_base + C::COL_ACC + cc * 32, a);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = 0u;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(a[8 * qd + 0]) * sc, __uint_as_float(a[8 * qd + 1]) * sc);
+            w.y = pack_bf16x2(__uint_as_float(a[8 * qd + 2]) * sc, __uint_as_float(a[8 * qd + 3]) * sc);
+            w.z = pack_bf16x2(__uint_as_float(a[8 * qd + 4]) * sc, __uint_as_float(a[8 * qd + 5]) * sc);
+            w.w = pack_bf16x2(__uint_as_float(a[8 * qd + 6]) * sc, __uint_as_float(a[8 * qd + 7]) * sc);
+            *reinterpret_cast<uint4*>(drow + cc * 32 + 8 * qd) = w;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one 128-key tile per CTA, looping over the stacked query tiles
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwParams p) {
+  using C = BwCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + C::OFF_FIX;
+  uint8_t* sV = sK + C::TILE_BYTES;
+  uint8_t* sRing = smem + C::OFF_RING;  // stage s: Q at s * 2 * TILE, dO right after
+  BwBars* bars = reinterpret_cast<BwBars*>(smem + C::OFF_BAR);
+  float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [2 buffers][lse2 | D][128]
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int kt = blockIdx.x;
+  const int bkv = blockIdx.y;
+  const int b = bkv / p.Hkv;
+  const int kvh = bkv % p.Hkv;
+  const int shift = p.S - p.T;
+  const int key0 = kt * C::BN;
+  // query tiles that see any key of this tile: position pos sees key0 iff key0 <= pos + shift
+  int qt0 = 0;
+  if (p.causal) qt0 = max(0, key0 - shift) / p.rows_per_head;
+  const int nsteps = max(0, p.n_qtiles - qt0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->fix_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->ring_full[s], 1);
+      mbar_init(&bars->ring_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->e_done, 128);
+    mbar_init(&bars->acc_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort_flag = &bars->abort_flag;
+  const uint64_t tmo = p.timeout_ns;
+  auto fail = [&](unsigned site) {
+    record_error(p.err, FA_ERR_TIMEOUT, site);
+    *abort_flag = 1;
+  };
+
+  if (warp == C::PRODUCER_WARP) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->fix_full, 2 * C::TILE_BYTES);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_3d(sK + c * C::CHUNK_BYTES, &tmK, &bars->fix_full, c * 64, key0, bkv);
+        tma_load_3d(sV + c * C::CHUNK_BYTES, &tmV, &bars->fix_full, c * 64, key0, bkv);
+      }
+      int issued = 0;
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !mbar_wait(&bars->ring_empty[s], ((i >> 1) - 1) & 1, tmo, abort_flag)) {
+          fail(SITE_BW_PRODUCER);
+          break;
+        }
+        uint8_t* st = sRing + s * 2 * C::TILE_BYTES;
+        const int qt = qt0 + i;
+        mbar_arrive_expect_tx(&bars->ring_full[s], 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d(st + c * C::CHUNK_BYTES, &tmQ, &bars->ring_full[s], c * 64, qt * p.rows_per_head, kvh * p.g, b);
+          tma_load_4d(st + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmDO, &bars->ring_full[s], c * 64,
+                      qt * p.rows_per_head, kvh * p.g, b);
+        }
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait(&bars->fix_full, 0, tmo);
+        for (int x = max(0, issued - 2); x < issued; ++x) mbar_wait(&bars->ring_full[x & 1], (x >> 1) & 1, tmo);
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    const bool leader = elect_one();
+    constexpr uint32_t idesc_ss = idesc_bf16_f32(128, C::BN, 0, 0);
+    constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, 0, 1);
+    const uint64_t dKd = smem_desc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t dVd = smem_desc_sw128(smem_u32(sV), 16, 1024);
+    const uint64_t dRingQ = smem_desc_sw128(smem_u32(sRing), 16, 1024);                          // Q as the B of S^T
+    const uint64_t dRingDO = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), 16, 1024);         // dO as the B of dP^T
+    const uint64_t dRingQmn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);            // Q as the B of dK
+    const uint64_t dRingDOmn = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), C::CHUNK_BYTES, 1024);  // dO for dV
+    bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
+    for (int i = 0; ok && i < nsteps; ++i) {
+      const int s = i & 1;
+      if (!mbar_wait(&bars->ring_full[s], (i >> 1) & 1, tmo, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t so = static_cast<uint64_t>((s * 2 * C::TILE_BYTES) >> 4);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + C::COL_S, dKd + off, dRingQ + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + C::COL_DP, dVd + off, dRingDO + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&bars->s_full);
+      }
+      if (!mbar_wait(&bars->e_done, i & 1, tmo, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
+        // dV += P^T dO (P^T over S^T's first 64 columns), dK += dS^T Q (dS^T over dP^T's)
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + kk * 8, dRingDOmn + so + static_cast<uint64_t>((kk * 2048) >> 4),
+                    idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          tc_mma_ts(tmem + C::COL_ACC + D, tmem + C::COL_DP + kk * 8,
+                    dRingQmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars->ring_empty[s]);
+      }
+    }
+    if (!ok && leader) fail(SITE_BW_MMA);
+    if (leader) tc_commit(&bars->acc_done);
+    mbar_wait(&bars->acc_done, 0, tmo);
+  } else {
+    // ---- elementwise warps: one key row per thread (TMEM lane); a step's 128
+    //      columns are the stacked query rows of one query tile
+    const int r = threadIdx.x;  // 0..127
+    const int key = key0 + r;
+    const bool key_valid = key < p.S;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::COL_S;
+    const uint32_t tDP = tmem + lane_base + C::COL_DP;
+    const float c = p.c;
+    bool ok = true;
+    for (int i = 0; i < nsteps; ++i) {
+      const int qt = qt0 + i;
+      // column r of this step: LSE (base 2) and D of stacked query row r
+      float* lse2v = vec + (i & 1) * 2 * C::BM;
+      float* dv_ = lse2v + C::BM;
+      {
+        int h_local, pos;
+        bw_row(p, qt, r, h_local, pos);
+        float l2 = INFINITY, dd = 0.f;  // rows past T: P = 0
+        if (pos < p.T) {
+          const size_t ri = (static_cast<size_t>(b) * p.Hq + kvh * p.g + h_local) * p.T + pos;
+          const float l = __ldg(p.lse + ri);
+          l2 = l == -INFINITY ? INFINITY : l * kLog2e;
+          dd = __ldg(p.dsum + ri);
+        }
+        lse2v[r] = l2;
+        dv_[r] = dd;
+      }
+      named_bar_sync(1, 128);  // the vectors of this step are complete (double-buffered by step parity)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, i & 1, tmo, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // column col is position qt * rows_per_head + (col & rmask) of head col / rows_per_head
+      // (rows_per_head = 128 / g is a power of two); the key is visible to it iff
+      // key <= position + shift, i.e. (col & rmask) >= vis_from
+      const int rmask = p.rows_per_head - 1;
+      const int vis_from = p.causal ? key - shift - qt * p.rows_per_head : INT_MIN;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + cc * 32, sr);
+        tmem_ld32(tDP + cc * 32, dr);
+        tmem_ld_wait();
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) {
+          float pv2[2], ds2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = cc * 32 + 2 * ii + e;
+            const bool vis = key_valid && (col & rmask) >= vis_from;  // keys past S masked too
+            const float pv = vis ? ex2_approx(fmaf(__uint_as_float(sr[2 * ii + e]), c, -lse2v[col])) : 0.f;
+            pv2[e] = pv;
+            ds2[e] = pv * (__uint_as_float(dr[2 * ii + e]) - dv_[col]);
+          }
+          pp[ii] = pack_bf16x2(pv2[0], pv2[1]);
+          pd[ii] = pack_bf16x2(ds2[0], ds2[1]);
+        }
+        tmem_st16(tS + cc * 16, pp);   // P^T over S^T's columns already read
+        tmem_st16(tDP + cc * 16, pd);  // dS^T over dP^T's
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->e_done);
+    }
+    if (!ok) fail(SITE_BW_ELEM);
+    // ---- epilogue: dV, dK = scale * (dS^T Q) -> bf16
+    if (ok && nsteps > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_done, 0, tmo, abort_flag));
+      tc_fence_after();
+    }
+    if (ok) {
+      const size_t krow = static_cast<size_t>(bkv) * p.S + (key_valid ? key : 0);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* drow = (which ? p.dk : p.dv) + krow * D;
+        const float sc = which ? p.scale : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t a[32];
+          if (nsteps > 0) {
+            tmem_ld32(tmem + lane_base + C::COL_ACC + which * D + cc * 32, a);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) a[ii] = 0u;
+          }
+          if (key_valid) {
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(a[8 * qd + 0]) * sc, __uint_as_float(a[8 * qd + 1]) * sc);
+              w.y = pack_bf16x2(__uint_as_float(a[8 * qd + 2]) * sc, __uint_as_float(a[8 * qd + 3]) * sc);
+              w.z = pack_bf16x2(__uint_as_float(a[8 * qd + 4]) * sc, __uint_as_float(a[8 * qd + 5]) * sc);
+              w.w = pack_bf16x2(__uint_as_float(a[8 * qd + 6]) * sc, __uint_as_float(a[8 * qd + 7]) * sc);
+              *reinterpret_cast<uint4*>(drow + cc * 32 + 8 * qd) = w;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+static bool encode_stacked(EncodeTiledFn enc, CUtensorMap* m, const void* base, int B, int Hq, int T, int d, int g,
+                           int rows_per_head) {
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)Hq, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2, (cuuint64_t)Hq * T * d * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)rows_per_head, (cuuint32_t)g, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool encode_keys(EncodeTiledFn enc, CUtensorMap* m, const void* base, int B, int Hkv, int S, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)B * Hkv};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+static int launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const BwParams& p, cudaStream_t stream) {
+  using C = BwCfg<D>;
+  auto kq = bwd_dq_kernel<D>;
+  auto kkv = bwd_dkdv_kernel<D>;
+  if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const unsigned nbkv = static_cast<unsigned>(p.B * p.Hkv);
+  kkv<<<dim3(p.n_ktiles, nbkv), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, p);
+  kq<<<dim3(p.n_qtiles, nbkv), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// q, o, d_o [B][Hq][T][d]; k, v [B][Hkv][S][d] bf16; lse [B][Hq][T] fp32; dsum:
+// B*Hq*T floats of scratch for D. Writes dq, dk, dv (bf16, shapes of q, k, v).
+int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
+                    void* dq, void* dk, void* dv, float* dsum, int B, int Hq, int Hkv, int T, int S, int d,
+                    float scale, int causal, cudaStream_t stream, unsigned* err, unsigned long long timeout_ns) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return FA_ERR_CUDA;
+  const int g = Hq / Hkv;
+  const int rows_per_head = 128 / g;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!encode_stacked(enc, &tq, q, B, Hq, T, d, g, rows_per_head) ||
+      !encode_stacked(enc, &tdo, d_o, B, Hq, T, d, g, rows_per_head) || !encode_keys(enc, &tk, k, B, Hkv, S, d) ||
+      !encode_keys(enc, &tv, v, B, Hkv, S, d))
+    return FA_ERR_CUDA;
+  const long long rows = static_cast<long long>(B) * Hq * T;
+  bwd_rowsum_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), dsum, rows, d);
+  BwParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.lse = lse;
+  p.dsum = dsum;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.S = S;
+  p.g = g;
+  p.rows_per_head = rows_per_head;
+  p.n_qtiles = (T + rows_per_head - 1) / rows_per_head;
+  p.n_ktiles = (S + 127) / 128;
+  p.causal = causal;
+  p.scale = scale;
+  p.c = scale * kLog2e;
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  return d == 128 ? launch_bwd_t<128>(tq, tdo, tk, tv, p, stream) : launch_bwd_t<64>(tq, tdo, tk, tv, p, stream);
+}
+
+}  // namespace fa

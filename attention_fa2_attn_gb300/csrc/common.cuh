@@ -26,6 +26,9 @@ enum ErrSite : unsigned {
   SITE_DEC_CONSUMER = 6,
   SITE_DEC_TABLE = 7,
   SITE_PF_TABLE = 8,
+  SITE_BW_PRODUCER = 9,
+  SITE_BW_MMA = 10,
+  SITE_BW_ELEM = 11,
 };
 
 __device__ __forceinline__ void record_error(unsigned* err, unsigned code, unsigned site) {

@@ -96,6 +96,31 @@ FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, floa
                      void* stream);
 
 /*
+ * fa_bwd -- gradients of the forward for an upstream gradient dO.
+ * ("Attention kernel chains", "What the backward pass saves": the forward keeps
+ *  Q, K, V, O and the fp32 log-sum-exp per query row; the backward rebuilds
+ *  each probability tile as P = exp(S - LSE) and needs D = rowsum(dO * O),
+ *  formed once before the main loops.) With S = scale * Q K^T:
+ *  dV = P^T dO, dP = dO V^T, dS = P * (dP - D), dQ = scale * dS K,
+ *  dK = scale * dS^T Q; a KV head's dK and dV sum over its group's query heads.
+ *   q, o, d_o [B][Hq][Tq][d] bf16; k, v [B][Hkv][Skv][d] bf16 (as fa_fwd);
+ *   lse [B][Hq][Tq] fp32, the forward's (natural log, -inf for keyless rows);
+ *   dq [B][Hq][Tq][d], dk, dv [B][Hkv][Skv][d] bf16 out (overwritten).
+ *   causal: the same bottom-right mask as fa_fwd. d in {64, 128}; Hq / Hkv in
+ *   {1, 2, 4, 8, 16}.
+ *   workspace: device scratch of at least fa_bwd_workspace_bytes(B, Hq, Tq)
+ *   bytes, 16-byte aligned, for D. Three launches on `stream`: D, then dK/dV
+ *   (one CTA per 128-key tile), then dQ (one CTA per 128-row query tile).
+ */
+FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq,
+                        int Skv, int d, float scale, int causal, void* workspace, size_t ws_bytes,
+                        void* stream);
+
+/* fa_bwd_workspace_bytes -- 4 * B * Hq * Tq (one fp32 D per query row); 0 for invalid sizes. */
+FA_API size_t fa_bwd_workspace_bytes(int B, int Hq, int Tq);
+
+/*
  * fa_num_splits_heuristic -- how many key ranges a decode step should use.
  * ("Attention kernel chains", "How many splits for decode": split so that
  *  batch x KV heads x splits fills at most one wave of SMs; no split once

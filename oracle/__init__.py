@@ -14,6 +14,7 @@ forms, or an independent brute force. No function is "parity unpinned".
 from .attention import (  # noqa: F401
     NEG_INF,
     attention_backward,
+    attention_backward_rows,
     attention_online,
     attention_online_normalized,
     attention_partials,

@@ -495,3 +495,49 @@ def attention_backward(q, k, v, do, scale: float, causal: bool = False, o=None, 
 def backward_rowsum(do, o):
     """D = rowsum(dO * O), one value per query row ([CHAIN] "What the backward pass saves")."""
     return (_as64(do) * _as64(o)).sum(axis=-1)
+
+
+def attention_backward_rows(q, k, v, do, o, lse, q_rows, k_rows, scale: float, causal: bool = False):
+    """The backward of ``attention_backward`` for samples of rows only.
+
+    Rows of dQ are independent of one another: dQ_i = scale * sum_j dS_ij k_j
+    needs only query row i against every key. A row of dK or dV needs its key
+    against every query row of every head in the group: dV_j = sum P_ij dO_i,
+    dK_j = scale * sum dS_ij q_i. Each sampled row is computed exactly in
+    O(rows * d) from the same formulas ([CHAIN] "What the backward pass saves").
+    q_rows: (b, h, i) query rows; k_rows: (b, hk, j) key rows.
+    Returns (dq [len(q_rows)][d], dk [len(k_rows)][d], dv [len(k_rows)][d]).
+    """
+    q, k, v, do, o, lse = _as64(q), _as64(k), _as64(v), _as64(do), _as64(o), _as64(lse)
+    B, Hq, Hkv, T, S, d = _check_shapes(q, k, v)
+    g = Hq // Hkv
+    dsum = {}
+
+    def dsum_of(b, h):
+        if (b, h) not in dsum:
+            dsum[(b, h)] = backward_rowsum(do[b, h], o[b, h])
+        return dsum[(b, h)]
+
+    dq = np.zeros((len(q_rows), d))
+    for n, (b, h, i) in enumerate(q_rows):
+        hk = kv_head_of(h, Hq, Hkv)
+        vis = np.array([visible(i, j, T, S, causal) for j in range(S)])
+        x = scale * (k[b, hk] @ q[b, h, i])
+        p = np.where(vis, np.exp(x - lse[b, h, i]), 0.0) if np.isfinite(lse[b, h, i]) else np.zeros(S)
+        dp = v[b, hk] @ do[b, h, i]
+        ds = p * (dp - dsum_of(b, h)[i])
+        dq[n] = scale * (ds @ k[b, hk])
+    dk = np.zeros((len(k_rows), d))
+    dv = np.zeros((len(k_rows), d))
+    for n, (b, hk, j) in enumerate(k_rows):
+        vis = np.array([visible(i, j, T, S, causal) for i in range(T)])
+        for h in range(hk * g, (hk + 1) * g):
+            x = scale * (q[b, h] @ k[b, hk, j])
+            live = np.isfinite(lse[b, h]) & vis
+            p = np.zeros(T)
+            p[live] = np.exp(x[live] - lse[b, h][live])
+            dp = do[b, h] @ v[b, hk, j]
+            ds = p * (dp - dsum_of(b, h))
+            dv[n] += p @ do[b, h]
+            dk[n] += scale * (ds @ q[b, h])
+    return dq, dk, dv

@@ -126,3 +126,19 @@ def test_planted_backward_mistakes_are_caught(monkeypatch):
                     failed = True
                     break
             assert failed, f"planted mistake not caught: {name}"
+
+
+def test_backward_rows_match_full():
+    """The sampled-row backward equals the full one on the rows it computes."""
+    for causal in (False, True):
+        q, k, v, do = _problem(2, 4, 2, 9, 7, 5, 9)
+        o, lse = oracle.attention_three_pass(q, k, v, 0.6, causal)
+        dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.6, causal, o=o, lse=lse)
+        qrows = [(0, 0, 0), (1, 3, 8), (0, 2, 4), (1, 1, 1)]
+        krows = [(0, 0, 0), (1, 1, 6), (0, 1, 3)]
+        rq, rk, rv = oracle.attention_backward_rows(q, k, v, do, o, lse, qrows, krows, 0.6, causal)
+        for n, (b, h, i) in enumerate(qrows):
+            assert np.allclose(rq[n], dq[b, h, i], atol=1e-13)
+        for n, (b, hk, j) in enumerate(krows):
+            assert np.allclose(rk[n], dk[b, hk, j], atol=1e-13)
+            assert np.allclose(rv[n], dv[b, hk, j], atol=1e-13)

@@ -67,13 +67,21 @@ struct BwCfg {
   static constexpr int OFF_BAR = OFF_RING + STAGES * 2 * TILE_BYTES;
   static constexpr int OFF_VEC = OFF_BAR + 256;  // dK/dV: per-step LSE and D of the query columns
   static constexpr int SMEM = OFF_VEC + 2 * 2 * BM * 4 + 1024;
-  static constexpr int THREADS = 192;            // warps 0-3 elementwise, 4 producer, 5 MMA
-  static constexpr int PRODUCER_WARP = 4;
-  static constexpr int MMA_WARP = 5;
+  // warps 0-7 elementwise: warp w takes TMEM lanes 32(w%4).. and column half w/4
+  // (every element is independent, so a pair splits a row's columns with no
+  // exchange); warp 8 producer, warp 9 MMA
+  static constexpr int THREADS = 320;
+  static constexpr int EW_THREADS = 256;
+  static constexpr int PRODUCER_WARP = 8;
+  static constexpr int MMA_WARP = 9;
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;                // S (or S^T): fp32; P / dS (bf16) later over it
   static constexpr int COL_DP = 128;             // dP (or dP^T)
   static constexpr int COL_ACC = 256;            // dQ, or dV then dK
+  // Packed bf16 operands (two per 32-bit column) written by column half hf over
+  // the first 32 of its own 64 fp32 columns: the 16 keys (or queries) of MMA
+  // K-step kk sit at column packed_col(kk) of the S (or dP) region.
+  static __device__ __forceinline__ uint32_t packed_col(int kk) { return 64 * (kk >> 2) + (kk & 3) * 8; }
 };
 
 struct BwParams {
@@ -116,7 +124,7 @@ __device__ __forceinline__ void bw_row(const BwParams& p, int qt, int r, int& h_
 // dQ: one stacked query tile per CTA, looping over key tiles
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwParams p) {
   using C = BwCfg<D>;
@@ -145,7 +153,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bars->ring_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->e_done, 128);
+    mbar_init(&bars->e_done, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -229,8 +237,8 @@ __global__ void __launch_bounds__(192, 1)
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + kk * 8, dRingKmn + so + static_cast<uint64_t>((kk * 2048) >> 4),
-                    idesc_ts, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + C::packed_col(kk),
+                    dRingKmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&bars->ring_empty[s]);
       }
     }
@@ -238,8 +246,9 @@ __global__ void __launch_bounds__(192, 1)
     if (leader) tc_commit(&bars->acc_done);
     mbar_wait(&bars->acc_done, 0, tmo);
   } else {
-    // ---- elementwise warps: one query row per thread (TMEM lane)
-    const int r = threadIdx.x;  // 0..127
+    // ---- elementwise warps: one query row per thread pair (TMEM lane), column half hf
+    const int r = threadIdx.x & 127;
+    const int hf = warp >> 2;
     int h_local, pos;
     bw_row(p, qt, r, h_local, pos);
     const bool row_valid = pos < p.T;
@@ -260,15 +269,18 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const int key0 = j * C::BN;
-      // last visible key of this row (bottom-right causal), relative to key0
+      const int key0 = j * C::BN + hf * 64;
+      // last visible key of this row (bottom-right causal), relative to this half's first key
       const int lim = (p.causal ? min(p.S - 1, pos + shift) : p.S - 1) - key0;
+      uint32_t sr[2][32], dr[2][32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + cc * 32, sr);
-        tmem_ld32(tDP + cc * 32, dr);
-        tmem_ld_wait();
+      for (int cc = 0; cc < 2; ++cc) {
+        tmem_ld32(tS + hf * 64 + cc * 32, sr[cc]);
+        tmem_ld32(tDP + hf * 64 + cc * 32, dr[cc]);
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -276,12 +288,12 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int col = cc * 32 + 2 * i + e;
-            const float pv = col > lim ? 0.f : ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), c, -lse2));
-            ds2[e] = pv * (__uint_as_float(dr[2 * i + e]) - d_row);
+            const float pv = col > lim ? 0.f : ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i + e]), c, -lse2));
+            ds2[e] = pv * (__uint_as_float(dr[cc][2 * i + e]) - d_row);
           }
           pk[i] = pack_bf16x2(ds2[0], ds2[1]);
         }
-        tmem_st16(tS + cc * 16, pk);  // keys 32cc .. +31 -> columns 16cc .. +15 (already read)
+        tmem_st16(tS + hf * 64 + cc * 16, pk);  // over this half's own columns, already read
       }
       tmem_st_wait();
       tc_fence_before();
@@ -294,14 +306,15 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
     }
     if (ok) {
-      // every lane loads (tcgen05.ld is warp-collective); rows past T store nothing
-      __nv_bfloat16* drow = p.dq + row_index * D;
+      // every lane loads (tcgen05.ld is warp-collective); rows past T store nothing;
+      // each column half writes D/2 columns
+      __nv_bfloat16* drow = p.dq + row_index * D + hf * (D / 2);
       const float sc = p.scale;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t a[32];
         if (nj > 0) {
-          tmem_ld32(tmem + lane_base + C::COL_ACC + cc * 32, a);
+          tmem_ld32(tmem + lane_base + C::COL_ACC + hf * (D / 2) + cc * 32, a);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(192, 1)
 // dK, dV: one 128-key tile per CTA, looping over the stacked query tiles
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwParams p) {
   using C = BwCfg<D>;
@@ -364,7 +377,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bars->ring_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->e_done, 128);
+    mbar_init(&bars->e_done, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -450,11 +463,11 @@ __global__ void __launch_bounds__(192, 1)
         // dV += P^T dO (P^T over S^T's first 64 columns), dK += dS^T Q (dS^T over dP^T's)
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + kk * 8, dRingDOmn + so + static_cast<uint64_t>((kk * 2048) >> 4),
-                    idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + C::packed_col(kk),
+                    dRingDOmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_ts(tmem + C::COL_ACC + D, tmem + C::COL_DP + kk * 8,
+          tc_mma_ts(tmem + C::COL_ACC + D, tmem + C::COL_DP + C::packed_col(kk),
                     dRingQmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&bars->ring_empty[s]);
       }
@@ -463,9 +476,10 @@ __global__ void __launch_bounds__(192, 1)
     if (leader) tc_commit(&bars->acc_done);
     mbar_wait(&bars->acc_done, 0, tmo);
   } else {
-    // ---- elementwise warps: one key row per thread (TMEM lane); a step's 128
-    //      columns are the stacked query rows of one query tile
-    const int r = threadIdx.x;  // 0..127
+    // ---- elementwise warps: one key row per thread pair (TMEM lane), column half
+    //      hf; a step's 128 columns are the stacked query rows of one query tile
+    const int r = threadIdx.x & 127;
+    const int hf = warp >> 2;
     const int key = key0 + r;
     const bool key_valid = key < p.S;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -478,7 +492,7 @@ __global__ void __launch_bounds__(192, 1)
       // column r of this step: LSE (base 2) and D of stacked query row r
       float* lse2v = vec + (i & 1) * 2 * C::BM;
       float* dv_ = lse2v + C::BM;
-      {
+      if (hf == 0) {
         int h_local, pos;
         bw_row(p, qt, r, h_local, pos);
         float l2 = INFINITY, dd = 0.f;  // rows past T: P = 0
@@ -491,7 +505,7 @@ __global__ void __launch_bounds__(192, 1)
         lse2v[r] = l2;
         dv_[r] = dd;
       }
-      named_bar_sync(1, 128);  // the vectors of this step are complete (double-buffered by step parity)
+      named_bar_sync(1, C::EW_THREADS);  // the vectors of this step are complete (double-buffered by step parity)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, i & 1, tmo, abort_flag))) {
         ok = false;
         break;
@@ -503,10 +517,10 @@ __global__ void __launch_bounds__(192, 1)
       const int rmask = p.rows_per_head - 1;
       const int vis_from = p.causal ? key - shift - qt * p.rows_per_head : INT_MIN;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t sr[32], dr[32];
-        tmem_ld32(tS + cc * 32, sr);
-        tmem_ld32(tDP + cc * 32, dr);
+        tmem_ld32(tS + hf * 64 + cc * 32, sr);
+        tmem_ld32(tDP + hf * 64 + cc * 32, dr);
         tmem_ld_wait();
         uint32_t pp[16], pd[16];
 #pragma unroll
@@ -514,7 +528,7 @@ __global__ void __launch_bounds__(192, 1)
           float pv2[2], ds2[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int col = cc * 32 + 2 * ii + e;
+            const int col = hf * 64 + cc * 32 + 2 * ii + e;
             const bool vis = key_valid && (col & rmask) >= vis_from;  // keys past S masked too
             const float pv = vis ? ex2_approx(fmaf(__uint_as_float(sr[2 * ii + e]), c, -lse2v[col])) : 0.f;
             pv2[e] = pv;
@@ -523,8 +537,8 @@ __global__ void __launch_bounds__(192, 1)
           pp[ii] = pack_bf16x2(pv2[0], pv2[1]);
           pd[ii] = pack_bf16x2(ds2[0], ds2[1]);
         }
-        tmem_st16(tS + cc * 16, pp);   // P^T over S^T's columns already read
-        tmem_st16(tDP + cc * 16, pd);  // dS^T over dP^T's
+        tmem_st16(tS + hf * 64 + cc * 16, pp);   // P^T over this half's own S^T columns, already read
+        tmem_st16(tDP + hf * 64 + cc * 16, pd);  // dS^T over its dP^T columns
       }
       tmem_st_wait();
       tc_fence_before();
@@ -540,13 +554,13 @@ __global__ void __launch_bounds__(192, 1)
       const size_t krow = static_cast<size_t>(bkv) * p.S + (key_valid ? key : 0);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* drow = (which ? p.dk : p.dv) + krow * D;
+        __nv_bfloat16* drow = (which ? p.dk : p.dv) + krow * D + hf * (D / 2);
         const float sc = which ? p.scale : 1.f;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
           uint32_t a[32];
           if (nsteps > 0) {
-            tmem_ld32(tmem + lane_base + C::COL_ACC + which * D + cc * 32, a);
+            tmem_ld32(tmem + lane_base + C::COL_ACC + which * D + hf * (D / 2) + cc * 32, a);
             tmem_ld_wait();
           } else {
 #pragma unroll

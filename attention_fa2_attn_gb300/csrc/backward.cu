@@ -106,8 +106,10 @@ struct BwBars {
   uint64_t fix_full;      // the fixed tile pair landed
   uint64_t ring_full[2];  // a ring stage (tile pair) landed
   uint64_t ring_empty[2]; // a ring stage's last reader finished
-  uint64_t s_full;        // S and dP (or S^T and dP^T) of this step are in TMEM
-  uint64_t e_done;        // the elementwise warps have written this step's operands
+  uint64_t s_full;        // S (or S^T) of this step is in TMEM
+  uint64_t dp_full;       // dP (or dP^T) of this step is in TMEM
+  uint64_t e_first;       // dQ: S read out of TMEM; dK/dV: P^T written
+  uint64_t e_second;      // dS (or dS^T) written
   uint64_t acc_done;      // the last accumulation finished
   uint32_t tmem_base;
   int abort_flag;
@@ -153,7 +155,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bars->ring_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->e_done, C::EW_THREADS);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->e_first, C::EW_THREADS);
+    mbar_init(&bars->e_second, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -206,10 +210,54 @@ __global__ void __launch_bounds__(320, 1)
     const uint64_t dRingK = smem_desc_sw128(smem_u32(sRing), 16, 1024);                   // K as the B of S
     const uint64_t dRingKmn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);     // K as the B of dQ
     const uint64_t dRingV = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), 16, 1024);   // V as the B of dP
+    // Issue order: S(0), dP(0), then per key tile j: S(j+1) (once the warps have read
+    // S(j) out), dQ(j) += dS(j) K_j (dS over dP's columns), dP(j+1) (after dQ(j) in
+    // issue order, so it never overwrites dS(j) before it is read). The MMAs of the
+    // neighbouring tiles run while the warps work on tile j.
+    auto issue_s = [&](int j) {
+      const uint64_t so = static_cast<uint64_t>(((j & 1) * 2 * C::TILE_BYTES) >> 4);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + C::COL_S, dQd + off, dRingK + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&bars->s_full);
+      }
+    };
+    auto issue_dp = [&](int j) {
+      const uint64_t so = static_cast<uint64_t>(((j & 1) * 2 * C::TILE_BYTES) >> 4);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + C::COL_DP, dDOd + off, dRingV + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&bars->dp_full);
+      }
+    };
     bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
+    if (ok && nj > 0) {
+      ok = mbar_wait(&bars->ring_full[0], 0, tmo, abort_flag);
+      tc_fence_after();
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+    }
     for (int j = 0; ok && j < nj; ++j) {
       const int s = j & 1;
-      if (!mbar_wait(&bars->ring_full[s], (j >> 1) & 1, tmo, abort_flag)) {
+      if (j + 1 < nj) {
+        // S(j+1) overwrites S(j): the warps must have read it out
+        if (!mbar_wait(&bars->e_first, j & 1, tmo, abort_flag) ||
+            !mbar_wait(&bars->ring_full[(j + 1) & 1], ((j + 1) >> 1) & 1, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(j + 1);
+      }
+      if (!mbar_wait(&bars->e_second, j & 1, tmo, abort_flag)) {
         ok = false;
         break;
       }
@@ -217,30 +265,12 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t so = static_cast<uint64_t>((s * 2 * C::TILE_BYTES) >> 4);
       if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_S, dQd + off, dRingK + so + off, idesc_ss, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_DP, dDOd + off, dRingV + so + off, idesc_ss, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&bars->s_full);
-      }
-      // dS (bf16, over S's first 64 columns) -> dQ += dS K
-      if (!mbar_wait(&bars->e_done, j & 1, tmo, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (leader) {
-#pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + C::packed_col(kk),
+          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_DP + C::packed_col(kk),
                     dRingKmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&bars->ring_empty[s]);
       }
+      if (j + 1 < nj) issue_dp(j + 1);
     }
     if (!ok && leader) fail(SITE_BW_MMA);
     if (leader) tc_commit(&bars->acc_done);
@@ -272,32 +302,39 @@ __global__ void __launch_bounds__(320, 1)
       const int key0 = j * C::BN + hf * 64;
       // last visible key of this row (bottom-right causal), relative to this half's first key
       const int lim = (p.causal ? min(p.S - 1, pos + shift) : p.S - 1) - key0;
-      uint32_t sr[2][32], dr[2][32];
+      // P = 2^(S*c - lse2) for this half's 64 keys, kept in registers; S is then free
+      float pv[64];
+      {
+        uint32_t sr[2][32];
+        tmem_ld32(tS + hf * 64, sr[0]);
+        tmem_ld32(tS + hf * 64 + 32, sr[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->e_first);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        tmem_ld32(tS + hf * 64 + cc * 32, sr[cc]);
-        tmem_ld32(tDP + hf * 64 + cc * 32, dr[cc]);
+        for (int i = 0; i < 64; ++i)
+          pv[i] = i > lim ? 0.f : ex2_approx(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, -lse2));
       }
-      tmem_ld_wait();
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, j & 1, tmo, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
+        uint32_t dr[32];
+        tmem_ld32(tDP + hf * 64 + cc * 32, dr);
+        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float ds2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = cc * 32 + 2 * i + e;
-            const float pv = col > lim ? 0.f : ex2_approx(fmaf(__uint_as_float(sr[cc][2 * i + e]), c, -lse2));
-            ds2[e] = pv * (__uint_as_float(dr[cc][2 * i + e]) - d_row);
-          }
-          pk[i] = pack_bf16x2(ds2[0], ds2[1]);
-        }
-        tmem_st16(tS + hf * 64 + cc * 16, pk);  // over this half's own columns, already read
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(pv[cc * 32 + 2 * i] * (__uint_as_float(dr[2 * i]) - d_row),
+                              pv[cc * 32 + 2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - d_row));
+        tmem_st16(tDP + hf * 64 + cc * 16, pk);  // dS over this half's own dP columns, already read
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->e_done);
+      mbar_arrive(&bars->e_second);
     }
     if (!ok) fail(SITE_BW_ELEM);
     // ---- epilogue: dQ = scale * (dS K) -> bf16
@@ -377,7 +414,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bars->ring_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->e_done, C::EW_THREADS);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->e_first, C::EW_THREADS);
+    mbar_init(&bars->e_second, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -432,45 +471,77 @@ __global__ void __launch_bounds__(320, 1)
     const uint64_t dRingDO = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), 16, 1024);         // dO as the B of dP^T
     const uint64_t dRingQmn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);            // Q as the B of dK
     const uint64_t dRingDOmn = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), C::CHUNK_BYTES, 1024);  // dO for dV
-    bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
-    for (int i = 0; ok && i < nsteps; ++i) {
-      const int s = i & 1;
-      if (!mbar_wait(&bars->ring_full[s], (i >> 1) & 1, tmo, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t so = static_cast<uint64_t>((s * 2 * C::TILE_BYTES) >> 4);
+    // Issue order: S^T(0), dP^T(0), then per query tile n: dV(n) += P^T(n) dO_n (P^T
+    // over S^T's columns), S^T(n+1), dK(n) += dS^T(n) Q_n (dS^T over dP^T's),
+    // dP^T(n+1). Each overwrite comes after the MMA that reads the region in issue
+    // order; the warps' P phase of tile n+1 runs under dK(n) and dP^T(n+1), their
+    // dS phase under dV(n+1) and S^T(n+2).
+    auto issue_s = [&](int n) {
+      const uint64_t so = static_cast<uint64_t>(((n & 1) * 2 * C::TILE_BYTES) >> 4);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
           tc_mma_ss(tmem + C::COL_S, dKd + off, dRingQ + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
+        tc_commit(&bars->s_full);
+      }
+    };
+    auto issue_dp = [&](int n) {
+      const uint64_t so = static_cast<uint64_t>(((n & 1) * 2 * C::TILE_BYTES) >> 4);
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
           tc_mma_ss(tmem + C::COL_DP, dVd + off, dRingDO + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&bars->s_full);
+        tc_commit(&bars->dp_full);
       }
-      if (!mbar_wait(&bars->e_done, i & 1, tmo, abort_flag)) {
+    };
+    bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
+    if (ok && nsteps > 0) {
+      ok = mbar_wait(&bars->ring_full[0], 0, tmo, abort_flag);
+      tc_fence_after();
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+    }
+    for (int i = 0; ok && i < nsteps; ++i) {
+      const int s = i & 1;
+      const uint64_t so = static_cast<uint64_t>((s * 2 * C::TILE_BYTES) >> 4);
+      if (!mbar_wait(&bars->e_first, i & 1, tmo, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (leader) {
-        // dV += P^T dO (P^T over S^T's first 64 columns), dK += dS^T Q (dS^T over dP^T's)
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + C::packed_col(kk),
                     dRingDOmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (i + 1 < nsteps) {
+        if (!mbar_wait(&bars->ring_full[(i + 1) & 1], ((i + 1) >> 1) & 1, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(i + 1);
+      }
+      if (!mbar_wait(&bars->e_second, i & 1, tmo, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           tc_mma_ts(tmem + C::COL_ACC + D, tmem + C::COL_DP + C::packed_col(kk),
                     dRingQmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&bars->ring_empty[s]);
       }
+      if (i + 1 < nsteps) issue_dp(i + 1);
     }
     if (!ok && leader) fail(SITE_BW_MMA);
     if (leader) tc_commit(&bars->acc_done);
@@ -516,33 +587,51 @@ __global__ void __launch_bounds__(320, 1)
       // key <= position + shift, i.e. (col & rmask) >= vis_from
       const int rmask = p.rows_per_head - 1;
       const int vis_from = p.causal ? key - shift - qt * p.rows_per_head : INT_MIN;
+      // P phase: P^T = 2^(S^T*c - lse2[col]) for this half's 64 query columns, kept in
+      // registers and written (bf16) over this half's own S^T columns
+      float pv[64];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t sr[32], dr[32];
+        uint32_t sr[32];
         tmem_ld32(tS + hf * 64 + cc * 32, sr);
-        tmem_ld32(tDP + hf * 64 + cc * 32, dr);
         tmem_ld_wait();
-        uint32_t pp[16], pd[16];
+        uint32_t pp[16];
 #pragma unroll
-        for (int ii = 0; ii < 16; ++ii) {
-          float pv2[2], ds2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = hf * 64 + cc * 32 + 2 * ii + e;
-            const bool vis = key_valid && (col & rmask) >= vis_from;  // keys past S masked too
-            const float pv = vis ? ex2_approx(fmaf(__uint_as_float(sr[2 * ii + e]), c, -lse2v[col])) : 0.f;
-            pv2[e] = pv;
-            ds2[e] = pv * (__uint_as_float(dr[2 * ii + e]) - dv_[col]);
-          }
-          pp[ii] = pack_bf16x2(pv2[0], pv2[1]);
-          pd[ii] = pack_bf16x2(ds2[0], ds2[1]);
+        for (int ii = 0; ii < 32; ++ii) {
+          const int col = hf * 64 + cc * 32 + ii;
+          const bool vis = key_valid && (col & rmask) >= vis_from;  // keys past S masked too
+          pv[cc * 32 + ii] = vis ? ex2_approx(fmaf(__uint_as_float(sr[ii]), c, -lse2v[col])) : 0.f;
         }
-        tmem_st16(tS + hf * 64 + cc * 16, pp);   // P^T over this half's own S^T columns, already read
-        tmem_st16(tDP + hf * 64 + cc * 16, pd);  // dS^T over its dP^T columns
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) pp[ii] = pack_bf16x2(pv[cc * 32 + 2 * ii], pv[cc * 32 + 2 * ii + 1]);
+        tmem_st16(tS + hf * 64 + cc * 16, pp);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->e_done);
+      mbar_arrive(&bars->e_first);
+      // dS phase: dS^T = P^T * (dP^T - D[col]) over this half's own dP^T columns
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, i & 1, tmo, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t dr[32];
+        tmem_ld32(tDP + hf * 64 + cc * 32, dr);
+        tmem_ld_wait();
+        uint32_t pd[16];
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) {
+          const int col = hf * 64 + cc * 32 + 2 * ii;
+          pd[ii] = pack_bf16x2(pv[cc * 32 + 2 * ii] * (__uint_as_float(dr[2 * ii]) - dv_[col]),
+                               pv[cc * 32 + 2 * ii + 1] * (__uint_as_float(dr[2 * ii + 1]) - dv_[col + 1]));
+        }
+        tmem_st16(tDP + hf * 64 + cc * 16, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->e_second);
     }
     if (!ok) fail(SITE_BW_ELEM);
     // ---- epilogue: dV, dK = scale * (dS^T Q) -> bf16

@@ -22,6 +22,13 @@ def attention_flops(B: int, Hq: int, T: int, S: int, d: int, causal: bool) -> fl
     return f / 2.0 if causal else f
 
 
+def attention_backward_flops(B: int, Hq: int, T: int, S: int, d: int, causal: bool) -> float:
+    """The backward's five products per (query, key) pair and head (S, dP, dV, dK, dQ),
+    2*d FLOP each: 2.5 times the forward's 4*T*S*d, halved for causal.
+    (The dQ kernel here recomputes S and dP, executing seven; the metric counts five.)"""
+    return 2.5 * attention_flops(B, Hq, T, S, d, causal)
+
+
 def visible_pairs(T: int, S: int, causal: bool) -> int:
     """(query, key) pairs the mask leaves visible for T queries over S keys.
 

@@ -375,6 +375,29 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
                    "seqlens": list(seqlens)}
     del q, kp, vp, table, sl, o, lse
 
+    # backward of the prefill workload (fa_bwd: D, dK/dV, dQ)
+    w = fi.PREFILL_MHA
+    q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)
+    k = rnd((w.B, w.Hkv, w.S, w.d), 2000 + w.index)
+    v = rnd((w.B, w.Hkv, w.S, w.d), 3000 + w.index)
+    d_o = rnd((w.B, w.Hq, w.T, w.d), 5000 + w.index)
+    o, lse = fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.Hq, w.T), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    step = lambda: fa.fa_bwd(q, k, v, o, lse, d_o, causal=w.causal, scale=w.scale, workspace=ws,  # noqa: E731
+                             dq=dq, dk=dk, dv=dv)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    bsteps = max(10, steps // 5)
+    ms = time_steps(torch, step, bsteps, stream)
+    tf = cm.attention_backward_flops(w.B, w.Hq, w.T, w.S, w.d, w.causal) / (ms * 1e-3) / 1e12
+    out["backward_" + w.name] = {"metric": "attn bwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                                 "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 3,
+                                 "steps": bsteps,
+                                 "flops": "2.5 x the forward's 4*T*S*d (S, dP, dV, dK, dQ); dQ's kernel recomputes S and dP"}
+    del q, k, v, d_o, o, lse, ws, dq, dk, dv
+
     # the prefill workload's one-head sweep: too few query tiles for 152 SMs, so the
     # keys are split (fa_num_splits_prefill) and the partials merged
     sms = torch.cuda.get_device_properties(dev).multi_processor_count

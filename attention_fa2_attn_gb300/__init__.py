@@ -15,6 +15,8 @@ from .api import (  # noqa: F401
     fa_decode_workspace_bytes,
     fa_fwd,
     fa_fwd_f32,
+    fa_fwd_kv_outer,
+    fa_fwd_kv_outer_workspace_bytes,
     fa_get_last_device_error,
     fa_lse_merge,
     fa_num_splits_heuristic,

@@ -37,6 +37,8 @@ SIGNATURES = {
     "fa_fwd_f32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "fa_fwd_kv_outer": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "fa_fwd_kv_outer_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_num_splits_heuristic": (_I, [_I, _I, _I, _I]),
     "fa_num_splits_prefill": (_I, [_I, _I, _I, _I, _I, _I]),
     "fa_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),

@@ -90,6 +90,32 @@ def fa_bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = Non
     return dq, dk, dv
 
 
+def fa_fwd_kv_outer_workspace_bytes(B: int, Hq: int, T: int, d: int) -> int:
+    return int(lib().fa_fwd_kv_outer_workspace_bytes(B, Hq, T, d))
+
+
+def fa_fwd_kv_outer(q, k, v, causal: bool = False, scale: float | None = None, row_bands: int = 1, workspace=None,
+                    out=None, lse=None):
+    """The forward in the FlashAttention-1 loop order (key tiles outer, running
+    state through HBM): q [B][Hq][T][d], k, v [B][Hkv][S][d] bf16 -> (o, lse)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Hq, T, d = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = fa_fwd_kv_outer_workspace_bytes(B, Hq, T, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = lib().fa_fwd_kv_outer(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
+                               int(causal), int(row_bands), _ptr(workspace), workspace.numel(), _stream(q))
+    check(st, "fa_fwd_kv_outer")
+    return o, lse
+
+
 def fa_num_splits_heuristic(B: int, Hkv: int, S: int, num_sms: int) -> int:
     return int(lib().fa_num_splits_heuristic(B, Hkv, S, num_sms))
 

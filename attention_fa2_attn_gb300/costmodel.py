@@ -87,6 +87,54 @@ def flash2_tile_bytes(N: int, d: int, e: int = 2, Br: int = 128, Bc: int = 128) 
     return moved, once
 
 
+def flash1_bytes(N: int, d: int, e: int = 2, Bc: int = 128, e_state: int = 4) -> float:
+    """FlashAttention-1 loop order, one head ("Kernel visualization: Flash Attention 1",
+    "Counting trips across HBM"): K and V read once; Q and the running O, m, l read
+    once per key tile, and O, m, l written back once per key tile (Tc = ceil(N / Bc)
+    key tiles). Q, K, V take e bytes a value, the running state e_state."""
+    tc = -(-N // Bc)
+    state = N * d * e_state + 2 * N * e_state  # O, m, l of every row
+    return 2 * N * d * e + tc * (N * d * e + 2 * state)
+
+
+def kv_outer_bytes(B: int, Hq: int, T: int, S: int, d: int, causal: bool = False, row_bands: int = 1, e: int = 2,
+                   Br: int = 128, Bc: int = 128) -> float:
+    """Bytes the FlashAttention-1-order kernel (fa_fwd_kv_outer) moves per launch,
+    counted over its loop nest with no reuse between CTAs. Each CTA loads every key
+    tile its band needs once (K and V). At each (key tile j, query tile i) step it
+    reads Q_i. Unless j is the tile's first key tile, it also reads the fp32 state
+    O', m, l. Unless j is the tile's last key tile (bottom-right causal mask), it
+    writes that state back; the last writes bf16 O and fp32 lse instead. A tile
+    that sees no key writes O = 0 and lse once."""
+    n_qt = -(-T // Br)
+    n_kt = -(-S // Bc)
+    R = max(1, min(row_bands, n_qt))
+    state = d * 4 + 8  # O', m, l of one row
+    final = d * e + 4  # O and lse of one row
+
+    def jmax(i):
+        if not causal:
+            return n_kt - 1
+        last_key = min(T, (i + 1) * Br) - 1 + S - T
+        return -1 if last_key < 0 else min(n_kt - 1, last_key // Bc)
+
+    per_head = 0
+    for band in range(R):
+        lo, hi = band * n_qt // R, (band + 1) * n_qt // R
+        band_jmax = -1
+        for i in range(lo, hi):
+            rows = min(T, (i + 1) * Br) - i * Br
+            jm = jmax(i)
+            band_jmax = max(band_jmax, jm)
+            if jm >= 0:
+                steps = jm + 1
+                per_head += steps * rows * d * e + 2 * (steps - 1) * rows * state
+            per_head += rows * final
+        for j in range(band_jmax + 1):
+            per_head += 2 * (min(S, (j + 1) * Bc) - j * Bc) * d * e
+    return float(per_head) * B * Hq
+
+
 def prefill_compulsory_bytes(B: int, Hq: int, Hkv: int, T: int, S: int, d: int, e: int = 2) -> float:
     """Q read, O written, K and V read once, fp32 lse written."""
     return e * (2 * B * Hq * T * d + 2 * B * Hkv * S * d) + 4 * B * Hq * T

@@ -30,6 +30,9 @@ int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float*
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
                     void* dq, void* dk, void* dv, float* dsum, int B, int Hq, int Hkv, int T, int S, int d,
                     float scale, int causal, cudaStream_t stream, unsigned* err, unsigned long long timeout_ns);
+int launch_kv_outer(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int T,
+                    int S, int d, float scale, int causal, int row_bands, void* workspace, cudaStream_t stream,
+                    unsigned* err, unsigned long long timeout_ns);
 
 // The device-side error word (code | site << 8). Kernels receive its device
 // address as a parameter.
@@ -211,6 +214,34 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
   int rc = launch_backward(q, k, v, o, lse, d_o, dq, dk, dv, static_cast<float*>(workspace), B, Hq, Hkv, Tq, Skv, d,
                            scale, causal ? 1 : 0, static_cast<cudaStream_t>(stream), err, g_timeout_ns);
+  if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
+  return static_cast<fa_status>(rc);
+}
+
+size_t fa_fwd_kv_outer_workspace_bytes(int B, int Hq, int Tq, int d) {
+  if (B <= 0 || Hq <= 0 || Tq <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * Tq;
+  return ((rows * d * 4 + 255) / 256) * 256 + 2 * rows * 4;
+}
+
+fa_status fa_fwd_kv_outer(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Tq, int Skv, int d, float scale, int causal, int row_bands, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Skv < 1 || Hq % Hkv != 0 || !good_scale(scale) || row_bands < 1)
+    return FA_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || ws_bytes < fa_fwd_kv_outer_workspace_bytes(B, Hq, Tq, d))
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const int g = Hq / Hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq * Tq >= (1ll << 31) || static_cast<long long>(B) * Hkv * Skv >= (1ll << 31))
+    return FA_ERR_UNSUPPORTED;
+  unsigned* err = error_word();
+  if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
+  int rc = launch_kv_outer(q, k, v, o, lse, B, Hq, Hkv, Tq, Skv, d, scale, causal ? 1 : 0, row_bands, workspace,
+                           static_cast<cudaStream_t>(stream), err, g_timeout_ns);
   if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
   return static_cast<fa_status>(rc);
 }

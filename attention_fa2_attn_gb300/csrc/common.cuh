@@ -1,5 +1,5 @@
 // common.cuh -- inline-PTX building blocks for the sm_103a kernels, written
-// from the PTX ISA: mbarriers with bounded waits, TMA (tensor and bulk) loads
+// from the PTX ISA: mbarriers with bounded waits, TMA tensor loads and stores
 // without multicast, tcgen05 TMEM allocation / MMA / loads / stores, fences,
 // and the device-side error word.
 #pragma once
@@ -29,6 +29,9 @@ enum ErrSite : unsigned {
   SITE_BW_PRODUCER = 9,
   SITE_BW_MMA = 10,
   SITE_BW_ELEM = 11,
+  SITE_KO_PRODUCER = 12,
+  SITE_KO_MMA = 13,
+  SITE_KO_UPDATE = 14,
 };
 
 __device__ __forceinline__ void record_error(unsigned* err, unsigned code, unsigned site) {
@@ -135,6 +138,21 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+
+// Tiled store smem -> global (rows past the tensor's extent are not written),
+// tracked by bulk async-groups of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed group of this thread has finished reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed group of this thread has completed (its global writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ----------------------------------------------------------------------------
 // Fences between the generic proxy (st.shared) and the async proxy (tensor core)

@@ -398,9 +398,48 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
                                  "flops": "2.5 x the forward's 4*T*S*d (S, dP, dV, dK, dQ); dQ's kernel recomputes S and dP"}
     del q, k, v, d_o, o, lse, ws, dq, dk, dv
 
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    # the FlashAttention-1 loop order on the prefill workload (fa_fwd_kv_outer): the
+    # running O', m, l of every query row cross HBM once per key tile; against the
+    # FlashAttention-2 order (fa_fwd) on the same inputs
+    w = fi.PREFILL_MHA
+    q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)
+    k = rnd((w.B, w.Hkv, w.S, w.d), 2000 + w.index)
+    v = rnd((w.B, w.Hkv, w.S, w.d), 3000 + w.index)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.T, device=dev)
+    ws = torch.empty(fa.fa_fwd_kv_outer_workspace_bytes(w.B, w.Hq, w.T, w.d), dtype=torch.uint8, device=dev)
+    flops = cm.attention_flops(w.B, w.Hq, w.T, w.S, w.d, w.causal)
+    fa1 = {}
+    ksteps = max(5, steps // 4)
+    for label, bands in (("one_cta_per_head", 1), ("bands_to_fill_sms", max(1, sms // (w.B * w.Hq)))):
+        step = lambda bands=bands: fa.fa_fwd_kv_outer(q, k, v, causal=w.causal, scale=w.scale,  # noqa: E731
+                                                      row_bands=bands, workspace=ws, out=o, lse=lse)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        ms = time_steps(torch, step, ksteps, stream)
+        byt = cm.kv_outer_bytes(w.B, w.Hq, w.T, w.S, w.d, w.causal, bands)
+        fa1[label] = {"row_bands": bands, "ctas": w.B * w.Hq * bands, "ms_per_step": ms,
+                      "TFLOP/s": flops / (ms * 1e-3) / 1e12, "bytes_per_step": byt,
+                      "GB/s": byt / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": byt / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                      "traffic": load_traffic().get("kv_outer_kernel_" + label) if bands == 1 else None}
+    step = lambda: fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)  # noqa: E731
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms2 = time_steps(torch, step, ksteps, stream)
+    out["fa1_order_" + w.name] = {
+        "metric": "attn fwd TFLOP/s", "unit": "TFLOP/s", "steps": ksteps, "launches_per_step": 1,
+        "fa1_order": fa1,
+        "fa2_order": {"ms_per_step": ms2, "TFLOP/s": flops / (ms2 * 1e-3) / 1e12,
+                      "compulsory_bytes_per_step": cm.prefill_compulsory_bytes(w.B, w.Hq, w.Hkv, w.T, w.S, w.d)},
+        "bytes": "kv_outer_bytes: the loop nest's HBM reads and writes, no reuse between CTAs assumed"}
+    del q, k, v, o, lse, ws
+
     # the prefill workload's one-head sweep: too few query tiles for 152 SMs, so the
     # keys are split (fa_num_splits_prefill) and the partials merged
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     sweep = {}
     for N, d in fi.PREFILL_MHA.sweep:
         q = rnd((1, 1, N, d), 1000 + fi.PREFILL_MHA.index)

@@ -121,6 +121,40 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
 FA_API size_t fa_bwd_workspace_bytes(int B, int Hq, int Tq);
 
 /*
+ * fa_fwd_kv_outer -- the operation of fa_fwd computed in the FlashAttention-1
+ * loop order, kept as a measured contrast to fa_fwd's order.
+ * ("Kernel visualization: Flash Attention 1", "The tiled version", "Kernel
+ *  implementation", "Counting trips across HBM": the key/value tiles form the
+ *  outer loop and the query tiles the inner one. Each (key tile, query tile) step
+ *  reads the query tile's running max m, sum l and normalised output O' from HBM,
+ *  folds the key tile in, and writes them back. Only the last key tile's step
+ *  leaves the final O. "Softmax and FlashAttention", "Concept": the
+ *  FlashAttention-2 order of fa_fwd reads each query tile and writes each output
+ *  tile once.)
+ *   q, k, v, o, lse, scale, causal: as fa_fwd. The same bottom-right mask applies.
+ *   row_bands: CTAs per (batch, query head), each running the loop nest over a
+ *   contiguous band of 128-row query tiles and loading every key tile once per
+ *   band. 1 gives the pages' grid, one CTA per (batch, head). Values above the
+ *   number of query tiles are clamped to it.
+ *   workspace: device scratch of at least fa_fwd_kv_outer_workspace_bytes(B, Hq,
+ *   Tq, d) bytes, 16-byte aligned. It holds the running O', m and l in fp32. The
+ *   first key tile of a query tile starts from m = -inf, l = 0, O' = 0 without
+ *   reading it, so it needs no initialisation.
+ *   d in {64, 128}; Hq / Hkv in {1, 2, 4, 8, 16}. Each query head's CTA loads its
+ *   KV head's tiles, without GQA stacking.
+ *   Errors: FA_ERR_INVALID_ARG for null or misaligned pointers, bad sizes, a
+ *   non-positive scale, row_bands < 1 or a workspace that is too small.
+ *   FA_ERR_UNSUPPORTED for other d or group sizes, or too many CTAs.
+ */
+FA_API fa_status fa_fwd_kv_outer(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int Hq, int Hkv, int Tq, int Skv, int d, float scale, int causal,
+                                 int row_bands, void* workspace, size_t ws_bytes, void* stream);
+
+/* fa_fwd_kv_outer_workspace_bytes -- O' (4 * B*Hq*Tq*d bytes, rounded up to 256)
+ * plus m and l (4 * B*Hq*Tq bytes each); 0 for invalid sizes. */
+FA_API size_t fa_fwd_kv_outer_workspace_bytes(int B, int Hq, int Tq, int d);
+
+/*
  * fa_num_splits_heuristic -- how many key ranges a decode step should use.
  * ("Attention kernel chains", "How many splits for decode": split so that
  *  batch x KV heads x splits fills at most one wave of SMs; no split once

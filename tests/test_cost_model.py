@@ -81,3 +81,33 @@ def test_visible_pairs_brute_force():
     # square causal: N(N+1)/2, the exact count behind the "halved" convention
     assert cm.visible_pairs(4096, 4096, True) == 4096 * 4097 // 2
     assert cm.chunked_attention_flops(2, 3, [3, 5], 8) == 4.0 * 2 * 8 * (6 + 12)
+
+
+def test_flash1_counting_trips():
+    """The FlashAttention-1 count with two key tiles ("Counting trips across HBM"):
+    K and V once, Q, O, m, l read twice, O, m, l written twice."""
+    N, d = 256, 64
+    e, es = 2, 4
+    state = N * d * es + 2 * N * es
+    assert cm.flash1_bytes(N, d, e, Bc=128, e_state=es) == 2 * N * d * e + 2 * N * d * e + 4 * state
+
+
+def test_kv_outer_bytes_against_the_page_count():
+    """Non-causal, one band: the kernel's count is the pages' FlashAttention-1 count
+    less the first key tile's state read and the last one's state write, plus the
+    final bf16 O and lse."""
+    for N, d in ((4096, 128), (1024, 64), (640, 128)):
+        state = N * (d * 4 + 8)
+        expect = cm.flash1_bytes(N, d, 2, 128, 4) - 2 * state + N * (2 * d + 4)
+        assert cm.kv_outer_bytes(1, 1, N, N, d) == expect
+        # bands reload K and V once each
+        assert cm.kv_outer_bytes(1, 1, N, N, d, row_bands=2) == expect + 2 * N * d * 2
+    # causal, T = S = 256: tile 0 needs key tile 0 only, tile 1 both
+    d = 64
+    got = cm.kv_outer_bytes(1, 1, 256, 256, d, causal=True)
+    q_reads = 3 * 128 * d * 2
+    state_io = 2 * 128 * (d * 4 + 8)  # tile 1: state out after key tile 0, in before key tile 1
+    assert got == q_reads + state_io + 256 * (2 * d + 4) + 2 * 256 * d * 2
+    # T > S: a tile no key reaches writes O = 0 and lse only
+    assert cm.kv_outer_bytes(1, 1, 256, 100, d, causal=True) == (
+        128 * (2 * d + 4) + 128 * d * 2 + 128 * (2 * d + 4) + 2 * 100 * d * 2)

@@ -113,3 +113,23 @@ def test_decode_rejects_bad_arguments(L):
     assert L.fa_decode_paged(*args) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_lse_merge(P, P, P, None, 0, 4, 128, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_lse_merge(P, P, P, None, 2, 4, 512, None) == _lib.FA_ERR_UNSUPPORTED
+
+
+def test_kv_outer_workspace_and_rejections(L):
+    rows, d = 2 * 4 * 100, 128
+    need = ((rows * d * 4 + 255) // 256) * 256 + 2 * rows * 4
+    assert L.fa_fwd_kv_outer_workspace_bytes(2, 4, 100, d) == need
+    assert L.fa_fwd_kv_outer_workspace_bytes(0, 4, 100, d) == 0
+
+    def ko(*, q=P, ws=P, ws_bytes=need, B=2, Hq=4, Hkv=2, T=100, S=300, d=128, scale=0.1, bands=1):
+        return L.fa_fwd_kv_outer(q, P, P, P, None, B, Hq, Hkv, T, S, d, scale, 1, bands, ws, ws_bytes, None)
+
+    assert ko(q=None) == _lib.FA_ERR_INVALID_ARG
+    assert ko(bands=0) == _lib.FA_ERR_INVALID_ARG
+    assert ko(ws=None) == _lib.FA_ERR_INVALID_ARG
+    assert ko(ws_bytes=need - 1) == _lib.FA_ERR_INVALID_ARG
+    assert ko(ws=MIS) == _lib.FA_ERR_INVALID_ARG
+    assert ko(scale=-1.0) == _lib.FA_ERR_INVALID_ARG
+    assert ko(Hq=3) == _lib.FA_ERR_INVALID_ARG
+    assert ko(d=96, ws_bytes=1 << 30) == _lib.FA_ERR_UNSUPPORTED
+    assert ko(Hq=12, Hkv=4, ws_bytes=1 << 30) == _lib.FA_ERR_UNSUPPORTED  # group of 3

@@ -291,7 +291,9 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::COL_S;
     const uint32_t tDP = tmem + lane_base + C::COL_DP;
-    const float c = p.c;
+    const float2 c2 = make_float2(p.c, p.c);
+    const float2 nl2 = make_float2(-lse2, -lse2);
+    const float2 nd2 = make_float2(-d_row, -d_row);
     bool ok = true;
     for (int j = 0; j < nj; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, tmo, abort_flag))) {
@@ -312,25 +314,40 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         mbar_arrive(&bars->e_first);
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          pv[i] = i > lim ? 0.f : ex2_approx(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, -lse2));
+        for (int i = 0; i < 64; i += 2) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[i >> 5][i & 31]), __uint_as_float(sr[i >> 5][(i & 31) + 1])),
+                                 c2, nl2);
+          pv[i] = ex2_approx(x.x);
+          pv[i + 1] = ex2_approx(x.y);
+        }
+        if (__any_sync(0xffffffffu, lim < 63)) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i > lim) pv[i] = 0.f;
+        }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, j & 1, tmo, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dr[32];
-        tmem_ld32(tDP + hf * 64 + cc * 32, dr);
+      {
+        uint32_t dr[2][32];
+        tmem_ld32(tDP + hf * 64, dr[0]);
+        tmem_ld32(tDP + hf * 64 + 32, dr[1]);
         tmem_ld_wait();
-        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(pv[cc * 32 + 2 * i] * (__uint_as_float(dr[2 * i]) - d_row),
-                              pv[cc * 32 + 2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - d_row));
-        tmem_st16(tDP + hf * 64 + cc * 16, pk);  // dS over this half's own dP columns, already read
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int e = cc * 32 + 2 * i;
+            const float2 t = fadd2(make_float2(__uint_as_float(dr[cc][2 * i]), __uint_as_float(dr[cc][2 * i + 1])), nd2);
+            const float2 g2 = fmul2(make_float2(pv[e], pv[e + 1]), t);
+            pk[i] = pack_bf16x2(g2.x, g2.y);
+          }
+          tmem_st16(tDP + hf * 64 + cc * 16, pk);  // dS over this half's own dP columns, already read
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -556,27 +573,38 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::COL_S;
     const uint32_t tDP = tmem + lane_base + C::COL_DP;
-    const float c = p.c;
-    bool ok = true;
-    for (int i = 0; i < nsteps; ++i) {
-      const int qt = qt0 + i;
-      // column r of this step: LSE (base 2) and D of stacked query row r
-      float* lse2v = vec + (i & 1) * 2 * C::BM;
-      float* dv_ = lse2v + C::BM;
-      if (hf == 0) {
+    const float2 c2 = make_float2(p.c, p.c);
+    const int rmask = p.rows_per_head - 1;
+    // column r of step i: -LSE in base 2 (-inf for rows past T or without a visible
+    // key: P = 0) and -D of stacked query row r, read by the first column half one
+    // step ahead so that the loads overlap the step before
+    auto load_vec = [&](int i, float& nl2, float& nd) {
+      nl2 = -INFINITY;
+      nd = 0.f;
+      if (i < nsteps) {
         int h_local, pos;
-        bw_row(p, qt, r, h_local, pos);
-        float l2 = INFINITY, dd = 0.f;  // rows past T: P = 0
+        bw_row(p, qt0 + i, r, h_local, pos);
         if (pos < p.T) {
           const size_t ri = (static_cast<size_t>(b) * p.Hq + kvh * p.g + h_local) * p.T + pos;
           const float l = __ldg(p.lse + ri);
-          l2 = l == -INFINITY ? INFINITY : l * kLog2e;
-          dd = __ldg(p.dsum + ri);
+          nl2 = l == -INFINITY ? -INFINITY : -l * kLog2e;
+          nd = -__ldg(p.dsum + ri);
         }
-        lse2v[r] = l2;
-        dv_[r] = dd;
       }
-      named_bar_sync(1, C::EW_THREADS);  // the vectors of this step are complete (double-buffered by step parity)
+    };
+    float nl2 = -INFINITY, nd = 0.f;
+    if (hf == 0) {
+      load_vec(0, nl2, nd);
+      vec[r] = nl2;
+      vec[C::BM + r] = nd;
+    }
+    bool ok = true;
+    for (int i = 0; i < nsteps; ++i) {
+      const int qt = qt0 + i;
+      const float* nl2v = vec + (i & 1) * 2 * C::BM + hf * 64;  // this half's 64 columns
+      const float* ndv = nl2v + C::BM;
+      named_bar_sync(1, C::EW_THREADS);  // this step's vectors are complete (double-buffered by step parity)
+      if (hf == 0) load_vec(i + 1, nl2, nd);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, i & 1, tmo, abort_flag))) {
         ok = false;
         break;
@@ -585,23 +613,41 @@ __global__ void __launch_bounds__(320, 1)
       // column col is position qt * rows_per_head + (col & rmask) of head col / rows_per_head
       // (rows_per_head = 128 / g is a power of two); the key is visible to it iff
       // key <= position + shift, i.e. (col & rmask) >= vis_from
-      const int rmask = p.rows_per_head - 1;
       const int vis_from = p.causal ? key - shift - qt * p.rows_per_head : INT_MIN;
+      const bool masked = !__all_sync(0xffffffffu, key_valid && vis_from <= 0);
       // P phase: P^T = 2^(S^T*c - lse2[col]) for this half's 64 query columns, kept in
       // registers and written (bf16) over this half's own S^T columns
       float pv[64];
+      {
+        uint32_t sr[2][32];
+        tmem_ld32(tS + hf * 64, sr[0]);
+        tmem_ld32(tS + hf * 64 + 32, sr[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nl2v + cc * 32 + 4 * q);
+            const int e = cc * 32 + 4 * q;
+            const float2 x0 = ffma2(make_float2(__uint_as_float(sr[cc][4 * q]), __uint_as_float(sr[cc][4 * q + 1])),
+                                    c2, make_float2(l4.x, l4.y));
+            const float2 x1 = ffma2(make_float2(__uint_as_float(sr[cc][4 * q + 2]), __uint_as_float(sr[cc][4 * q + 3])),
+                                    c2, make_float2(l4.z, l4.w));
+            pv[e] = ex2_approx(x0.x);
+            pv[e + 1] = ex2_approx(x0.y);
+            pv[e + 2] = ex2_approx(x1.x);
+            pv[e + 3] = ex2_approx(x1.y);
+          }
+        }
+      }
+      if (masked) {  // keys past S, or (causal) columns the key is not visible to
+#pragma unroll
+        for (int ii = 0; ii < 64; ++ii)
+          if (!(key_valid && ((hf * 64 + ii) & rmask) >= vis_from)) pv[ii] = 0.f;
+      }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t sr[32];
-        tmem_ld32(tS + hf * 64 + cc * 32, sr);
-        tmem_ld_wait();
         uint32_t pp[16];
-#pragma unroll
-        for (int ii = 0; ii < 32; ++ii) {
-          const int col = hf * 64 + cc * 32 + ii;
-          const bool vis = key_valid && (col & rmask) >= vis_from;  // keys past S masked too
-          pv[cc * 32 + ii] = vis ? ex2_approx(fmaf(__uint_as_float(sr[ii]), c, -lse2v[col])) : 0.f;
-        }
 #pragma unroll
         for (int ii = 0; ii < 16; ++ii) pp[ii] = pack_bf16x2(pv[cc * 32 + 2 * ii], pv[cc * 32 + 2 * ii + 1]);
         tmem_st16(tS + hf * 64 + cc * 16, pp);
@@ -615,23 +661,40 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dr[32];
-        tmem_ld32(tDP + hf * 64 + cc * 32, dr);
+      {
+        uint32_t dr[2][32];
+        tmem_ld32(tDP + hf * 64, dr[0]);
+        tmem_ld32(tDP + hf * 64 + 32, dr[1]);
         tmem_ld_wait();
-        uint32_t pd[16];
 #pragma unroll
-        for (int ii = 0; ii < 16; ++ii) {
-          const int col = hf * 64 + cc * 32 + 2 * ii;
-          pd[ii] = pack_bf16x2(pv[cc * 32 + 2 * ii] * (__uint_as_float(dr[2 * ii]) - dv_[col]),
-                               pv[cc * 32 + 2 * ii + 1] * (__uint_as_float(dr[2 * ii + 1]) - dv_[col + 1]));
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pd[16];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 d4 = *reinterpret_cast<const float4*>(ndv + cc * 32 + 4 * q);
+            const int e = cc * 32 + 4 * q;
+            const float2 t0 = fadd2(make_float2(__uint_as_float(dr[cc][4 * q]), __uint_as_float(dr[cc][4 * q + 1])),
+                                    make_float2(d4.x, d4.y));
+            const float2 t1 = fadd2(make_float2(__uint_as_float(dr[cc][4 * q + 2]), __uint_as_float(dr[cc][4 * q + 3])),
+                                    make_float2(d4.z, d4.w));
+            const float2 g0 = fmul2(make_float2(pv[e], pv[e + 1]), t0);
+            const float2 g1 = fmul2(make_float2(pv[e + 2], pv[e + 3]), t1);
+            pd[2 * q] = pack_bf16x2(g0.x, g0.y);
+            pd[2 * q + 1] = pack_bf16x2(g1.x, g1.y);
+          }
+          tmem_st16(tDP + hf * 64 + cc * 16, pd);
         }
-        tmem_st16(tDP + hf * 64 + cc * 16, pd);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->e_second);
+      // the next step's vectors into the other buffer: its last readers (step i-1)
+      // passed this step's barrier above
+      if (hf == 0) {
+        float* nb = vec + ((i + 1) & 1) * 2 * C::BM;
+        nb[r] = nl2;
+        nb[C::BM + r] = nd;
+      }
     }
     if (!ok) fail(SITE_BW_ELEM);
     // ---- epilogue: dV, dK = scale * (dS^T Q) -> bf16

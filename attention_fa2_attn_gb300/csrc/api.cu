@@ -28,7 +28,7 @@ int launch_decode(const void* q, const void* k, const void* v, const int* block_
 int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows, int d,
                      cudaStream_t stream);
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
-                    void* dq, void* dk, void* dv, float* dsum, int B, int Hq, int Hkv, int T, int S, int d,
+                    void* dq, void* dk, void* dv, float* vecs, int B, int Hq, int Hkv, int T, int S, int d,
                     float scale, int causal, cudaStream_t stream, unsigned* err, unsigned long long timeout_ns);
 int launch_kv_outer(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int T,
                     int S, int d, float scale, int causal, int row_bands, void* workspace, cudaStream_t stream,
@@ -41,8 +41,11 @@ __device__ unsigned g_fa_device_error;
 static thread_local char g_cuda_err[256] = "no error";
 static unsigned long long g_timeout_ns = 4000000000ull;
 
+// Keeps the text of a CUDA error for fa_last_cuda_error_string; cudaSuccess (the
+// error was already consumed and recorded where it happened) keeps the old text.
 static int cuda_fail(cudaError_t e) {
-  snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  if (e != cudaSuccess)
+    snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
   return FA_ERR_CUDA;
 }
 
@@ -190,7 +193,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int T) {
   if (B <= 0 || Hq <= 0 || T <= 0) return 0;
-  return static_cast<size_t>(B) * Hq * T * 4;
+  const size_t t_pad = (static_cast<size_t>(T) + 3) / 4 * 4;
+  return 2 * static_cast<size_t>(B) * Hq * t_pad * 4;
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,

@@ -29,11 +29,14 @@
 namespace fa {
 
 // ---------------------------------------------------------------------------
-// D = rowsum(dO * O): one warp per row
+// Per query row, into the row-vector workspace [2][B*Hq][T_pad]: -D = -rowsum(dO * O)
+// (plane 0) and -lse * log2(e), the row's LSE in base 2 negated (plane 1; -inf for
+// a row with no visible key, so that its P is 0). One warp per row.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) bwd_rowsum_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ d_o,
-                                                         float* __restrict__ dsum, long long rows, int d) {
+                                                         const float* __restrict__ lse, float* __restrict__ vecs,
+                                                         long long rows, int T, int T_pad, int d) {
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -47,7 +50,14 @@ __global__ void __launch_bounds__(256) bwd_rowsum_kernel(const __nv_bfloat16* __
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dsum[row] = acc;
+  if (lane == 0) {
+    const long long bh = row / T;
+    const long long at = bh * T_pad + (row - bh * T);
+    const long long plane = (rows / T) * T_pad;
+    const float l = lse[row];
+    vecs[at] = -acc;
+    vecs[plane + at] = l == -INFINITY ? -INFINITY : -l * kLog2e;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -65,7 +75,7 @@ struct BwCfg {
   static constexpr int OFF_FIX = 0;
   static constexpr int OFF_RING = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * 2 * TILE_BYTES;
-  static constexpr int OFF_VEC = OFF_BAR + 256;  // dK/dV: per-step LSE and D of the query columns
+  static constexpr int OFF_VEC = OFF_BAR + 256;  // dK/dV: per ring stage, -lse2 and -D of the query columns
   static constexpr int SMEM = OFF_VEC + 2 * 2 * BM * 4 + 1024;
   // warps 0-7 elementwise: warp w takes TMEM lanes 32(w%4).. and column half w/4
   // (every element is independent, so a pair splits a row's columns with no
@@ -88,8 +98,9 @@ struct BwParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
-  const float* lse;   // [B][Hq][T], natural log
-  const float* dsum;  // D = rowsum(dO * O), [B][Hq][T]
+  const float* neg_d;  // -D per query row, [B*Hq][T_pad]
+  const float* nl2;    // -lse * log2(e) per query row (-inf: no visible key), [B*Hq][T_pad]
+  int T_pad;           // T rounded up to a multiple of 4 (16-byte rows for TMA)
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -285,15 +296,15 @@ __global__ void __launch_bounds__(320, 1)
     const int h = kvh * p.g + h_local;
     const size_t row_index = (static_cast<size_t>(b) * p.Hq + h) * p.T + (row_valid ? pos : 0);
     // P = 2^(S*c - lse*log2e); rows past T and rows with no visible key get P = 0
-    const float lse_row = row_valid ? __ldg(p.lse + row_index) : -INFINITY;
-    const float lse2 = lse_row == -INFINITY ? INFINITY : lse_row * kLog2e;
-    const float d_row = row_valid ? __ldg(p.dsum + row_index) : 0.f;
+    const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.T_pad + (row_valid ? pos : 0);
+    const float nl2_row = row_valid ? __ldg(p.nl2 + vi) : -INFINITY;
+    const float nd_row = row_valid ? __ldg(p.neg_d + vi) : 0.f;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::COL_S;
     const uint32_t tDP = tmem + lane_base + C::COL_DP;
     const float2 c2 = make_float2(p.c, p.c);
-    const float2 nl2 = make_float2(-lse2, -lse2);
-    const float2 nd2 = make_float2(-d_row, -d_row);
+    const float2 nl2 = make_float2(nl2_row, nl2_row);
+    const float2 nd2 = make_float2(nd_row, nd_row);
     bool ok = true;
     for (int j = 0; j < nj; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, tmo, abort_flag))) {
@@ -402,7 +413,8 @@ __global__ void __launch_bounds__(320, 1)
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwParams p) {
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmVec, const BwParams p) {
   using C = BwCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -410,7 +422,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sV = sK + C::TILE_BYTES;
   uint8_t* sRing = smem + C::OFF_RING;  // stage s: Q at s * 2 * TILE, dO right after
   BwBars* bars = reinterpret_cast<BwBars*>(smem + C::OFF_BAR);
-  float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [2 buffers][lse2 | D][128]
+  float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // per ring stage: [-lse2 | -D][128]
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int kt = blockIdx.x;
@@ -465,12 +477,16 @@ __global__ void __launch_bounds__(320, 1)
         }
         uint8_t* st = sRing + s * 2 * C::TILE_BYTES;
         const int qt = qt0 + i;
-        mbar_arrive_expect_tx(&bars->ring_full[s], 2 * C::TILE_BYTES);
+        mbar_arrive_expect_tx(&bars->ring_full[s], 2 * C::TILE_BYTES + 2 * C::BM * 4);
         for (int c = 0; c < C::KCH; ++c) {
           tma_load_4d(st + c * C::CHUNK_BYTES, &tmQ, &bars->ring_full[s], c * 64, qt * p.rows_per_head, kvh * p.g, b);
           tma_load_4d(st + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmDO, &bars->ring_full[s], c * 64,
                       qt * p.rows_per_head, kvh * p.g, b);
         }
+        // the tile's -lse2 (plane B + b) and -D (plane b) in stacked row order;
+        // positions past T read as 0 (their Q and dO rows are zero as well)
+        tma_load_3d(vec + s * 2 * C::BM, &tmVec, &bars->ring_full[s], qt * p.rows_per_head, kvh * p.g, p.B + b);
+        tma_load_3d(vec + s * 2 * C::BM + C::BM, &tmVec, &bars->ring_full[s], qt * p.rows_per_head, kvh * p.g, b);
         issued = i + 1;
       }
       if (*abort_flag) {
@@ -575,37 +591,14 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tDP = tmem + lane_base + C::COL_DP;
     const float2 c2 = make_float2(p.c, p.c);
     const int rmask = p.rows_per_head - 1;
-    // column r of step i: -LSE in base 2 (-inf for rows past T or without a visible
-    // key: P = 0) and -D of stacked query row r, read by the first column half one
-    // step ahead so that the loads overlap the step before
-    auto load_vec = [&](int i, float& nl2, float& nd) {
-      nl2 = -INFINITY;
-      nd = 0.f;
-      if (i < nsteps) {
-        int h_local, pos;
-        bw_row(p, qt0 + i, r, h_local, pos);
-        if (pos < p.T) {
-          const size_t ri = (static_cast<size_t>(b) * p.Hq + kvh * p.g + h_local) * p.T + pos;
-          const float l = __ldg(p.lse + ri);
-          nl2 = l == -INFINITY ? -INFINITY : -l * kLog2e;
-          nd = -__ldg(p.dsum + ri);
-        }
-      }
-    };
-    float nl2 = -INFINITY, nd = 0.f;
-    if (hf == 0) {
-      load_vec(0, nl2, nd);
-      vec[r] = nl2;
-      vec[C::BM + r] = nd;
-    }
     bool ok = true;
     for (int i = 0; i < nsteps; ++i) {
       const int qt = qt0 + i;
+      // this step's -lse2 and -D of the 128 query columns came with its Q and dO tiles
       const float* nl2v = vec + (i & 1) * 2 * C::BM + hf * 64;  // this half's 64 columns
       const float* ndv = nl2v + C::BM;
-      named_bar_sync(1, C::EW_THREADS);  // this step's vectors are complete (double-buffered by step parity)
-      if (hf == 0) load_vec(i + 1, nl2, nd);
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, i & 1, tmo, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->ring_full[i & 1], (i >> 1) & 1, tmo, abort_flag) &&
+                                       mbar_wait(&bars->s_full, i & 1, tmo, abort_flag))) {
         ok = false;
         break;
       }
@@ -688,13 +681,6 @@ __global__ void __launch_bounds__(320, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->e_second);
-      // the next step's vectors into the other buffer: its last readers (step i-1)
-      // passed this step's barrier above
-      if (hf == 0) {
-        float* nb = vec + ((i + 1) & 1) * 2 * C::BM;
-        nb[r] = nl2;
-        nb[C::BM + r] = nd;
-      }
     }
     if (!ok) fail(SITE_BW_ELEM);
     // ---- epilogue: dV, dK = scale * (dS^T Q) -> bf16
@@ -772,7 +758,7 @@ static bool encode_keys(EncodeTiledFn enc, CUtensorMap* m, const void* base, int
 
 template <int D>
 static int launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const BwParams& p, cudaStream_t stream) {
+                        const CUtensorMap& tvec, const BwParams& p, cudaStream_t stream) {
   using C = BwCfg<D>;
   auto kq = bwd_dq_kernel<D>;
   auto kkv = bwd_dkdv_kernel<D>;
@@ -780,15 +766,16 @@ static int launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo, const CUt
       cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
   const unsigned nbkv = static_cast<unsigned>(p.B * p.Hkv);
-  kkv<<<dim3(p.n_ktiles, nbkv), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, p);
+  kkv<<<dim3(p.n_ktiles, nbkv), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, tvec, p);
   kq<<<dim3(p.n_qtiles, nbkv), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_status();
 }
 
-// q, o, d_o [B][Hq][T][d]; k, v [B][Hkv][S][d] bf16; lse [B][Hq][T] fp32; dsum:
-// B*Hq*T floats of scratch for D. Writes dq, dk, dv (bf16, shapes of q, k, v).
+// q, o, d_o [B][Hq][T][d]; k, v [B][Hkv][S][d] bf16; lse [B][Hq][T] fp32; vecs:
+// 2 * B*Hq*T_pad floats of scratch for the row vectors (T_pad = T rounded up to 4).
+// Writes dq, dk, dv (bf16, shapes of q, k, v).
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
-                    void* dq, void* dk, void* dv, float* dsum, int B, int Hq, int Hkv, int T, int S, int d,
+                    void* dq, void* dk, void* dv, float* vecs, int B, int Hq, int Hkv, int T, int S, int d,
                     float scale, int causal, cudaStream_t stream, unsigned* err, unsigned long long timeout_ns) {
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return FA_ERR_CUDA;
@@ -799,15 +786,29 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
       !encode_stacked(enc, &tdo, d_o, B, Hq, T, d, g, rows_per_head) || !encode_keys(enc, &tk, k, B, Hkv, S, d) ||
       !encode_keys(enc, &tv, v, B, Hkv, S, d))
     return FA_ERR_CUDA;
+  const int T_pad = (T + 3) / 4 * 4;
+  CUtensorMap tvec;
+  {
+    // planes: -D of batch b at b, -lse2 of batch b at B + b; rows T_pad floats apart
+    cuuint64_t dims[3] = {(cuuint64_t)T, (cuuint64_t)Hq, (cuuint64_t)2 * B};
+    cuuint64_t strides[2] = {(cuuint64_t)T_pad * 4, (cuuint64_t)Hq * T_pad * 4};
+    cuuint32_t box[3] = {(cuuint32_t)rows_per_head, (cuuint32_t)g, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tvec, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, vecs, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FA_ERR_CUDA;
+  }
   const long long rows = static_cast<long long>(B) * Hq * T;
   bwd_rowsum_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), dsum, rows, d);
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, vecs, rows, T, T_pad, d);
   BwParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
-  p.lse = lse;
-  p.dsum = dsum;
+  p.neg_d = vecs;
+  p.nl2 = vecs + static_cast<size_t>(B) * Hq * T_pad;
+  p.T_pad = T_pad;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
@@ -825,7 +826,8 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
   p.c = scale * kLog2e;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  return d == 128 ? launch_bwd_t<128>(tq, tdo, tk, tv, p, stream) : launch_bwd_t<64>(tq, tdo, tk, tv, p, stream);
+  return d == 128 ? launch_bwd_t<128>(tq, tdo, tk, tv, tvec, p, stream)
+                  : launch_bwd_t<64>(tq, tdo, tk, tv, tvec, p, stream);
 }
 
 }  // namespace fa

@@ -341,6 +341,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Host side: the status of the launches just made -- FA_OK, or FA_ERR_CUDA with the
+// error's text kept for fa_last_cuda_error_string (record_cuda_failure, api.cu).
+int record_cuda_failure(cudaError_t e);
+inline int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : record_cuda_failure(e);
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

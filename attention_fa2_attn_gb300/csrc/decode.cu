@@ -514,7 +514,7 @@ static int launch_lse_merge_impl(const float* o_part, const float* lse_part, voi
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
   if (cudaLaunchKernelEx(&cfg, lse_merge_kernel, o_part, lse_part, ob, lse, n, rows, d) != cudaSuccess)
     return FA_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_status();
 }
 
 int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows, int d,
@@ -532,7 +532,7 @@ static int launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const D
     return FA_ERR_CUDA;
   dim3 grid(nsplit, nbh);
   kfn<<<grid, C::THREADS, C::SMEM, stream>>>(tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_status();
 }
 
 // Shared by the contiguous and the paged entry points. `k`/`v` are either

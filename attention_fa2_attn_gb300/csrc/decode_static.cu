@@ -61,7 +61,6 @@ static void* static_scratch_address(cudaError_t* why) {
   return addr[dev];
 }
 
-int record_cuda_failure(cudaError_t e);  // api.cu: keeps the text for fa_last_cuda_error_string
 
 }  // namespace fa
 

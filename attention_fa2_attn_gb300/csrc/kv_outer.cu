@@ -612,7 +612,7 @@ int launch_kv_outer(const void* q, const void* k, const void* v, void* o, float*
       return FA_ERR_CUDA;
     kfn<<<static_cast<int>(grid), KoCfg<64>::THREADS, KoCfg<64>::SMEM, stream>>>(tq, tk, tv, to, p);
   }
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace fa

@@ -156,7 +156,7 @@ int launch_prefill_f32(const float* q, const float* k, const float* v, float* o,
   dim3 grid((T + F32_BR - 1) / F32_BR, B * Hq);
   if (grid.y > 65535u) return FA_ERR_UNSUPPORTED;
   prefill_f32_kernel<<<grid, 128, smem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace fa

@@ -744,7 +744,7 @@ static int launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                            PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
   kfn<<<grid, PfCfg<D>::THREADS, PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_status();
 }
 
 // Contiguous K/V ([B][Hkv][S][d]) when block_table is null; otherwise `k`/`v` are

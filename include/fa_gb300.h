@@ -35,7 +35,8 @@
  *     records a code in a device-side error word and the kernel returns.
  *     fa_get_last_device_error() reads and clears that word.
  *   - The library allocates no device memory. Scratch space (split-KV
- *     partials) is passed in by the caller as `workspace`.
+ *     partials, the backward's per-row values, the running state of the
+ *     FlashAttention-1 order) is passed in by the caller as `workspace`.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -109,7 +110,8 @@ FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, floa
  *   causal: the same bottom-right mask as fa_fwd. d in {64, 128}; Hq / Hkv in
  *   {1, 2, 4, 8, 16}.
  *   workspace: device scratch of at least fa_bwd_workspace_bytes(B, Hq, Tq)
- *   bytes, 16-byte aligned, for D. Three launches on `stream`: D, then dK/dV
+ *   bytes, 16-byte aligned, for two fp32 values per query row: -D and the LSE in
+ *   base 2, negated. Three launches on `stream`: those row values, then dK/dV
  *   (one CTA per 128-key tile), then dQ (one CTA per 128-row query tile).
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -117,7 +119,8 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
                         int Skv, int d, float scale, int causal, void* workspace, size_t ws_bytes,
                         void* stream);
 
-/* fa_bwd_workspace_bytes -- 4 * B * Hq * Tq (one fp32 D per query row); 0 for invalid sizes. */
+/* fa_bwd_workspace_bytes -- 8 * B * Hq * Tq', Tq' = Tq rounded up to a multiple of 4
+ * (two fp32 values per query row, rows padded to 16 bytes); 0 for invalid sizes. */
 FA_API size_t fa_bwd_workspace_bytes(int B, int Hq, int Tq);
 
 /*

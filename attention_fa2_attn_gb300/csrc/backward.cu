@@ -122,6 +122,8 @@ struct BwBars {
   uint64_t e_first;       // dQ: S read out of TMEM; dK/dV: P^T written
   uint64_t e_second;      // dS (or dS^T) written
   uint64_t acc_done;      // the last accumulation finished
+  uint64_t slot_full[4];  // dQ kernel: a K or V tile landed in ring slot t
+  uint64_t slot_empty[4]; // dQ kernel: the last MMA reading slot t finished
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -132,6 +134,12 @@ __device__ __forceinline__ void bw_row(const BwParams& p, int qt, int r, int& h_
   h_local = r / p.rows_per_head;
   pos = qt * p.rows_per_head + (r % p.rows_per_head);
 }
+
+// dQ kernel ring: four tile slots. Key tile j's K and V use the two slots of pair
+// j & 1, swapped every other use, so that K(j+2) lands in V(j)'s slot: V is free
+// once dP(j) has read it, well before dQ(j) releases K(j).
+__device__ __forceinline__ int dq_kslot(int j) { return 2 * (j & 1) + ((j >> 1) & 1); }
+__device__ __forceinline__ int dq_vslot(int j) { return 2 * (j & 1) + 1 - ((j >> 1) & 1); }
 
 // ---------------------------------------------------------------------------
 // dQ: one stacked query tile per CTA, looping over key tiles
@@ -170,6 +178,10 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bars->e_first, C::EW_THREADS);
     mbar_init(&bars->e_second, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
+    for (int t = 0; t < 4; ++t) {
+      mbar_init(&bars->slot_full[t], 1);
+      mbar_init(&bars->slot_empty[t], 1);
+    }
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -191,25 +203,40 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_4d(sQ + c * C::CHUNK_BYTES, &tmQ, &bars->fix_full, c * 64, qt * p.rows_per_head, kvh * p.g, b);
         tma_load_4d(sDO + c * C::CHUNK_BYTES, &tmDO, &bars->fix_full, c * 64, qt * p.rows_per_head, kvh * p.g, b);
       }
-      int issued = 0;
+      int issued = 0;  // tiles whose K and V loads were both issued
+      int k_only = -1;  // a tile whose K load was issued alone
       for (int j = 0; j < nj; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&bars->ring_empty[s], ((j >> 1) - 1) & 1, tmo, abort_flag)) {
+        // each slot's previous use was key tile j - 2
+        const int ks = dq_kslot(j), vs = dq_vslot(j);
+        const uint32_t prev = ((j >> 1) - 1) & 1;
+        if (j >= 2 && !mbar_wait(&bars->slot_empty[ks], prev, tmo, abort_flag)) {
           fail(SITE_BW_PRODUCER);
           break;
         }
-        uint8_t* st = sRing + s * 2 * C::TILE_BYTES;
-        mbar_arrive_expect_tx(&bars->ring_full[s], 2 * C::TILE_BYTES);
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_3d(st + c * C::CHUNK_BYTES, &tmK, &bars->ring_full[s], c * 64, j * C::BN, bkv);
-          tma_load_3d(st + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->ring_full[s], c * 64, j * C::BN, bkv);
+        mbar_arrive_expect_tx(&bars->slot_full[ks], C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(sRing + ks * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK, &bars->slot_full[ks], c * 64,
+                      j * C::BN, bkv);
+        k_only = j;
+        if (j >= 2 && !mbar_wait(&bars->slot_empty[vs], prev, tmo, abort_flag)) {
+          fail(SITE_BW_PRODUCER);
+          break;
         }
+        mbar_arrive_expect_tx(&bars->slot_full[vs], C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(sRing + vs * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV, &bars->slot_full[vs], c * 64,
+                      j * C::BN, bkv);
+        k_only = -1;
         issued = j + 1;
       }
       if (*abort_flag) {
         // copies in flight must land before the CTA exits
         mbar_wait(&bars->fix_full, 0, tmo);
-        for (int x = max(0, issued - 2); x < issued; ++x) mbar_wait(&bars->ring_full[x & 1], (x >> 1) & 1, tmo);
+        for (int x = max(0, issued - 2); x < issued; ++x) {
+          mbar_wait(&bars->slot_full[dq_kslot(x)], (x >> 1) & 1, tmo);
+          mbar_wait(&bars->slot_full[dq_vslot(x)], (x >> 1) & 1, tmo);
+        }
+        if (k_only >= 0) mbar_wait(&bars->slot_full[dq_kslot(k_only)], (k_only >> 1) & 1, tmo);
       }
     }
   } else if (warp == C::MMA_WARP) {
@@ -218,38 +245,42 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, 0, 1);      // A from TMEM, B MN-major
     const uint64_t dQd = smem_desc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dDOd = smem_desc_sw128(smem_u32(sDO), 16, 1024);
-    const uint64_t dRingK = smem_desc_sw128(smem_u32(sRing), 16, 1024);                   // K as the B of S
+    const uint64_t dRing = smem_desc_sw128(smem_u32(sRing), 16, 1024);                    // K (for S), V (for dP)
     const uint64_t dRingKmn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);     // K as the B of dQ
-    const uint64_t dRingV = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), 16, 1024);   // V as the B of dP
+    auto slot_off = [](int t) { return static_cast<uint64_t>((t * C::TILE_BYTES) >> 4); };
     // Issue order: S(0), dP(0), then per key tile j: S(j+1) (once the warps have read
     // S(j) out), dQ(j) += dS(j) K_j (dS over dP's columns), dP(j+1) (after dQ(j) in
     // issue order, so it never overwrites dS(j) before it is read). The MMAs of the
     // neighbouring tiles run while the warps work on tile j.
     auto issue_s = [&](int j) {
-      const uint64_t so = static_cast<uint64_t>(((j & 1) * 2 * C::TILE_BYTES) >> 4);
+      const uint64_t so = slot_off(dq_kslot(j));
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_S, dQd + off, dRingK + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tmem + C::COL_S, dQd + off, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
         tc_commit(&bars->s_full);
       }
     };
+    // dP(j); V(j)'s slot is free once it completes
     auto issue_dp = [&](int j) {
-      const uint64_t so = static_cast<uint64_t>(((j & 1) * 2 * C::TILE_BYTES) >> 4);
+      const int vs = dq_vslot(j);
+      const uint64_t so = slot_off(vs);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_DP, dDOd + off, dRingV + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tmem + C::COL_DP, dDOd + off, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
         tc_commit(&bars->dp_full);
+        tc_commit(&bars->slot_empty[vs]);
       }
     };
     bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
     if (ok && nj > 0) {
-      ok = mbar_wait(&bars->ring_full[0], 0, tmo, abort_flag);
+      ok = mbar_wait(&bars->slot_full[dq_kslot(0)], 0, tmo, abort_flag) &&
+           mbar_wait(&bars->slot_full[dq_vslot(0)], 0, tmo, abort_flag);
       tc_fence_after();
       if (ok) {
         issue_s(0);
@@ -257,11 +288,11 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     for (int j = 0; ok && j < nj; ++j) {
-      const int s = j & 1;
+      const uint32_t use_next = ((j + 1) >> 1) & 1;  // slot parity of key tile j + 1
       if (j + 1 < nj) {
         // S(j+1) overwrites S(j): the warps must have read it out
         if (!mbar_wait(&bars->e_first, j & 1, tmo, abort_flag) ||
-            !mbar_wait(&bars->ring_full[(j + 1) & 1], ((j + 1) >> 1) & 1, tmo, abort_flag)) {
+            !mbar_wait(&bars->slot_full[dq_kslot(j + 1)], use_next, tmo, abort_flag)) {
           ok = false;
           break;
         }
@@ -273,15 +304,23 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-      const uint64_t so = static_cast<uint64_t>((s * 2 * C::TILE_BYTES) >> 4);
+      const int ks = dq_kslot(j);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_DP + C::packed_col(kk),
-                    dRingKmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&bars->ring_empty[s]);
+                    dRingKmn + slot_off(ks) + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars->slot_empty[ks]);
       }
-      if (j + 1 < nj) issue_dp(j + 1);
+      if (j + 1 < nj) {
+        if (!mbar_wait(&bars->slot_full[dq_vslot(j + 1)], use_next, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_dp(j + 1);
+      }
     }
     if (!ok && leader) fail(SITE_BW_MMA);
     if (leader) tc_commit(&bars->acc_done);

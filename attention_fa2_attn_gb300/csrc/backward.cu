@@ -115,15 +115,13 @@ struct BwParams {
 
 struct BwBars {
   uint64_t fix_full;      // the fixed tile pair landed
-  uint64_t ring_full[2];  // a ring stage (tile pair) landed
-  uint64_t ring_empty[2]; // a ring stage's last reader finished
   uint64_t s_full;        // S (or S^T) of this step is in TMEM
   uint64_t dp_full;       // dP (or dP^T) of this step is in TMEM
   uint64_t e_first;       // dQ: S read out of TMEM; dK/dV: P^T written
   uint64_t e_second;      // dS (or dS^T) written
   uint64_t acc_done;      // the last accumulation finished
-  uint64_t slot_full[4];  // dQ kernel: a K or V tile landed in ring slot t
-  uint64_t slot_empty[4]; // dQ kernel: the last MMA reading slot t finished
+  uint64_t slot_full[4];  // a streamed tile landed in ring slot t
+  uint64_t slot_empty[4]; // the last MMA reading slot t finished
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -135,11 +133,13 @@ __device__ __forceinline__ void bw_row(const BwParams& p, int qt, int r, int& h_
   pos = qt * p.rows_per_head + (r % p.rows_per_head);
 }
 
-// dQ kernel ring: four tile slots. Key tile j's K and V use the two slots of pair
-// j & 1, swapped every other use, so that K(j+2) lands in V(j)'s slot: V is free
-// once dP(j) has read it, well before dQ(j) releases K(j).
-__device__ __forceinline__ int dq_kslot(int j) { return 2 * (j & 1) + ((j >> 1) & 1); }
-__device__ __forceinline__ int dq_vslot(int j) { return 2 * (j & 1) + 1 - ((j >> 1) & 1); }
+// The ring of both kernels: four tile slots. Step j's two streamed tiles use the
+// two slots of pair j & 1, swapped every other use: the tile whose last reader comes
+// late in the step (K in the dQ kernel, read by dQ; Q in the dK/dV kernel, read by
+// dK) lands in the slot that the other tile of step j - 2 (V, read last by dP; dO,
+// read last by dV) gave back early.
+__device__ __forceinline__ int slot_late(int j) { return 2 * (j & 1) + ((j >> 1) & 1); }
+__device__ __forceinline__ int slot_early(int j) { return 2 * (j & 1) + 1 - ((j >> 1) & 1); }
 
 // ---------------------------------------------------------------------------
 // dQ: one stacked query tile per CTA, looping over key tiles
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_FIX;
   uint8_t* sDO = sQ + C::TILE_BYTES;
-  uint8_t* sRing = smem + C::OFF_RING;  // stage s: K at s * 2 * TILE, V right after
+  uint8_t* sRing = smem + C::OFF_RING;  // four tile slots (slot_late / slot_early) for K and V
   BwBars* bars = reinterpret_cast<BwBars*>(smem + C::OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -169,10 +169,6 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->fix_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->ring_full[s], 1);
-      mbar_init(&bars->ring_empty[s], 1);
-    }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->e_first, C::EW_THREADS);
@@ -207,7 +203,7 @@ __global__ void __launch_bounds__(320, 1)
       int k_only = -1;  // a tile whose K load was issued alone
       for (int j = 0; j < nj; ++j) {
         // each slot's previous use was key tile j - 2
-        const int ks = dq_kslot(j), vs = dq_vslot(j);
+        const int ks = slot_late(j), vs = slot_early(j);
         const uint32_t prev = ((j >> 1) - 1) & 1;
         if (j >= 2 && !mbar_wait(&bars->slot_empty[ks], prev, tmo, abort_flag)) {
           fail(SITE_BW_PRODUCER);
@@ -233,10 +229,10 @@ __global__ void __launch_bounds__(320, 1)
         // copies in flight must land before the CTA exits
         mbar_wait(&bars->fix_full, 0, tmo);
         for (int x = max(0, issued - 2); x < issued; ++x) {
-          mbar_wait(&bars->slot_full[dq_kslot(x)], (x >> 1) & 1, tmo);
-          mbar_wait(&bars->slot_full[dq_vslot(x)], (x >> 1) & 1, tmo);
+          mbar_wait(&bars->slot_full[slot_late(x)], (x >> 1) & 1, tmo);
+          mbar_wait(&bars->slot_full[slot_early(x)], (x >> 1) & 1, tmo);
         }
-        if (k_only >= 0) mbar_wait(&bars->slot_full[dq_kslot(k_only)], (k_only >> 1) & 1, tmo);
+        if (k_only >= 0) mbar_wait(&bars->slot_full[slot_late(k_only)], (k_only >> 1) & 1, tmo);
       }
     }
   } else if (warp == C::MMA_WARP) {
@@ -253,7 +249,7 @@ __global__ void __launch_bounds__(320, 1)
     // issue order, so it never overwrites dS(j) before it is read). The MMAs of the
     // neighbouring tiles run while the warps work on tile j.
     auto issue_s = [&](int j) {
-      const uint64_t so = slot_off(dq_kslot(j));
+      const uint64_t so = slot_off(slot_late(j));
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -265,7 +261,7 @@ __global__ void __launch_bounds__(320, 1)
     };
     // dP(j); V(j)'s slot is free once it completes
     auto issue_dp = [&](int j) {
-      const int vs = dq_vslot(j);
+      const int vs = slot_early(j);
       const uint64_t so = slot_off(vs);
       if (leader) {
 #pragma unroll
@@ -279,8 +275,8 @@ __global__ void __launch_bounds__(320, 1)
     };
     bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
     if (ok && nj > 0) {
-      ok = mbar_wait(&bars->slot_full[dq_kslot(0)], 0, tmo, abort_flag) &&
-           mbar_wait(&bars->slot_full[dq_vslot(0)], 0, tmo, abort_flag);
+      ok = mbar_wait(&bars->slot_full[slot_late(0)], 0, tmo, abort_flag) &&
+           mbar_wait(&bars->slot_full[slot_early(0)], 0, tmo, abort_flag);
       tc_fence_after();
       if (ok) {
         issue_s(0);
@@ -292,7 +288,7 @@ __global__ void __launch_bounds__(320, 1)
       if (j + 1 < nj) {
         // S(j+1) overwrites S(j): the warps must have read it out
         if (!mbar_wait(&bars->e_first, j & 1, tmo, abort_flag) ||
-            !mbar_wait(&bars->slot_full[dq_kslot(j + 1)], use_next, tmo, abort_flag)) {
+            !mbar_wait(&bars->slot_full[slot_late(j + 1)], use_next, tmo, abort_flag)) {
           ok = false;
           break;
         }
@@ -304,7 +300,7 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-      const int ks = dq_kslot(j);
+      const int ks = slot_late(j);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
@@ -314,7 +310,7 @@ __global__ void __launch_bounds__(320, 1)
         tc_commit(&bars->slot_empty[ks]);
       }
       if (j + 1 < nj) {
-        if (!mbar_wait(&bars->slot_full[dq_vslot(j + 1)], use_next, tmo, abort_flag)) {
+        if (!mbar_wait(&bars->slot_full[slot_early(j + 1)], use_next, tmo, abort_flag)) {
           ok = false;
           break;
         }
@@ -459,7 +455,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem + C::OFF_FIX;
   uint8_t* sV = sK + C::TILE_BYTES;
-  uint8_t* sRing = smem + C::OFF_RING;  // stage s: Q at s * 2 * TILE, dO right after
+  uint8_t* sRing = smem + C::OFF_RING;  // four tile slots (slot_late / slot_early) for Q and dO
   BwBars* bars = reinterpret_cast<BwBars*>(smem + C::OFF_BAR);
   float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // per ring stage: [-lse2 | -D][128]
   const int warp = threadIdx.x >> 5;
@@ -477,15 +473,15 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->fix_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->ring_full[s], 1);
-      mbar_init(&bars->ring_empty[s], 1);
-    }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->e_first, C::EW_THREADS);
     mbar_init(&bars->e_second, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
+    for (int t = 0; t < 4; ++t) {
+      mbar_init(&bars->slot_full[t], 1);
+      mbar_init(&bars->slot_empty[t], 1);
+    }
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -507,30 +503,48 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sK + c * C::CHUNK_BYTES, &tmK, &bars->fix_full, c * 64, key0, bkv);
         tma_load_3d(sV + c * C::CHUNK_BYTES, &tmV, &bars->fix_full, c * 64, key0, bkv);
       }
-      int issued = 0;
+      int issued = 0;   // steps whose Q and dO loads were both issued
+      int q_only = -1;  // a step whose Q load was issued alone
       for (int i = 0; i < nsteps; ++i) {
-        const int s = i & 1;
-        if (i >= 2 && !mbar_wait(&bars->ring_empty[s], ((i >> 1) - 1) & 1, tmo, abort_flag)) {
+        // each slot's previous use was step i - 2
+        const int qs = slot_late(i), ds = slot_early(i);
+        const uint32_t prev = ((i >> 1) - 1) & 1;
+        const int qt = qt0 + i;
+        if (i >= 2 && !mbar_wait(&bars->slot_empty[qs], prev, tmo, abort_flag)) {
           fail(SITE_BW_PRODUCER);
           break;
         }
-        uint8_t* st = sRing + s * 2 * C::TILE_BYTES;
-        const int qt = qt0 + i;
-        mbar_arrive_expect_tx(&bars->ring_full[s], 2 * C::TILE_BYTES + 2 * C::BM * 4);
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_4d(st + c * C::CHUNK_BYTES, &tmQ, &bars->ring_full[s], c * 64, qt * p.rows_per_head, kvh * p.g, b);
-          tma_load_4d(st + C::TILE_BYTES + c * C::CHUNK_BYTES, &tmDO, &bars->ring_full[s], c * 64,
+        mbar_arrive_expect_tx(&bars->slot_full[qs], C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(sRing + qs * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, &bars->slot_full[qs], c * 64,
                       qt * p.rows_per_head, kvh * p.g, b);
+        q_only = i;
+        if (i >= 2 && !mbar_wait(&bars->slot_empty[ds], prev, tmo, abort_flag)) {
+          fail(SITE_BW_PRODUCER);
+          break;
         }
-        // the tile's -lse2 (plane B + b) and -D (plane b) in stacked row order;
-        // positions past T read as 0 (their Q and dO rows are zero as well)
-        tma_load_3d(vec + s * 2 * C::BM, &tmVec, &bars->ring_full[s], qt * p.rows_per_head, kvh * p.g, p.B + b);
-        tma_load_3d(vec + s * 2 * C::BM + C::BM, &tmVec, &bars->ring_full[s], qt * p.rows_per_head, kvh * p.g, b);
+        // dO, and the tile's -lse2 (plane B + b) and -D (plane b) in stacked row order
+        // (positions past T read as 0; their Q and dO rows are zero as well). The
+        // vectors' buffer i & 1 was last read by the warps in step i - 2, before dK(i - 2)
+        // and so before this slot came back.
+        mbar_arrive_expect_tx(&bars->slot_full[ds], C::TILE_BYTES + 2 * C::BM * 4);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(sRing + ds * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmDO, &bars->slot_full[ds], c * 64,
+                      qt * p.rows_per_head, kvh * p.g, b);
+        tma_load_3d(vec + (i & 1) * 2 * C::BM, &tmVec, &bars->slot_full[ds], qt * p.rows_per_head, kvh * p.g,
+                    p.B + b);
+        tma_load_3d(vec + (i & 1) * 2 * C::BM + C::BM, &tmVec, &bars->slot_full[ds], qt * p.rows_per_head,
+                    kvh * p.g, b);
+        q_only = -1;
         issued = i + 1;
       }
       if (*abort_flag) {
         mbar_wait(&bars->fix_full, 0, tmo);
-        for (int x = max(0, issued - 2); x < issued; ++x) mbar_wait(&bars->ring_full[x & 1], (x >> 1) & 1, tmo);
+        for (int x = max(0, issued - 2); x < issued; ++x) {
+          mbar_wait(&bars->slot_full[slot_late(x)], (x >> 1) & 1, tmo);
+          mbar_wait(&bars->slot_full[slot_early(x)], (x >> 1) & 1, tmo);
+        }
+        if (q_only >= 0) mbar_wait(&bars->slot_full[slot_late(q_only)], (q_only >> 1) & 1, tmo);
       }
     }
   } else if (warp == C::MMA_WARP) {
@@ -539,40 +553,40 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, 0, 1);
     const uint64_t dKd = smem_desc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t dVd = smem_desc_sw128(smem_u32(sV), 16, 1024);
-    const uint64_t dRingQ = smem_desc_sw128(smem_u32(sRing), 16, 1024);                          // Q as the B of S^T
-    const uint64_t dRingDO = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), 16, 1024);         // dO as the B of dP^T
-    const uint64_t dRingQmn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);            // Q as the B of dK
-    const uint64_t dRingDOmn = smem_desc_sw128(smem_u32(sRing + C::TILE_BYTES), C::CHUNK_BYTES, 1024);  // dO for dV
+    const uint64_t dRing = smem_desc_sw128(smem_u32(sRing), 16, 1024);               // Q (for S^T), dO (for dP^T)
+    const uint64_t dRingMn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);  // Q (for dK), dO (for dV)
+    auto slot_off = [](int t) { return static_cast<uint64_t>((t * C::TILE_BYTES) >> 4); };
     // Issue order: S^T(0), dP^T(0), then per query tile n: dV(n) += P^T(n) dO_n (P^T
     // over S^T's columns), S^T(n+1), dK(n) += dS^T(n) Q_n (dS^T over dP^T's),
     // dP^T(n+1). Each overwrite comes after the MMA that reads the region in issue
     // order; the warps' P phase of tile n+1 runs under dK(n) and dP^T(n+1), their
-    // dS phase under dV(n+1) and S^T(n+2).
+    // dS phase under dV(n+1) and S^T(n+2). dV(n) gives dO_n's slot back, dK(n) Q_n's.
     auto issue_s = [&](int n) {
-      const uint64_t so = static_cast<uint64_t>(((n & 1) * 2 * C::TILE_BYTES) >> 4);
+      const uint64_t so = slot_off(slot_late(n));
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_S, dKd + off, dRingQ + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tmem + C::COL_S, dKd + off, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
         tc_commit(&bars->s_full);
       }
     };
     auto issue_dp = [&](int n) {
-      const uint64_t so = static_cast<uint64_t>(((n & 1) * 2 * C::TILE_BYTES) >> 4);
+      const uint64_t so = slot_off(slot_early(n));
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_DP, dVd + off, dRingDO + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+          tc_mma_ss(tmem + C::COL_DP, dVd + off, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
         tc_commit(&bars->dp_full);
       }
     };
     bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
     if (ok && nsteps > 0) {
-      ok = mbar_wait(&bars->ring_full[0], 0, tmo, abort_flag);
+      ok = mbar_wait(&bars->slot_full[slot_late(0)], 0, tmo, abort_flag) &&
+           mbar_wait(&bars->slot_full[slot_early(0)], 0, tmo, abort_flag);
       tc_fence_after();
       if (ok) {
         issue_s(0);
@@ -580,21 +594,23 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     for (int i = 0; ok && i < nsteps; ++i) {
-      const int s = i & 1;
-      const uint64_t so = static_cast<uint64_t>((s * 2 * C::TILE_BYTES) >> 4);
+      const uint32_t use_next = ((i + 1) >> 1) & 1;  // slot parity of step i + 1
       if (!mbar_wait(&bars->e_first, i & 1, tmo, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (leader) {
+        const int ds = slot_early(i);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + C::packed_col(kk),
-                    dRingDOmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
+                    dRingMn + slot_off(ds) + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars->slot_empty[ds]);
       }
       if (i + 1 < nsteps) {
-        if (!mbar_wait(&bars->ring_full[(i + 1) & 1], ((i + 1) >> 1) & 1, tmo, abort_flag)) {
+        if (!mbar_wait(&bars->slot_full[slot_late(i + 1)], use_next, tmo, abort_flag)) {
           ok = false;
           break;
         }
@@ -607,13 +623,22 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_after();
       if (leader) {
+        const int qs = slot_late(i);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           tc_mma_ts(tmem + C::COL_ACC + D, tmem + C::COL_DP + C::packed_col(kk),
-                    dRingQmn + so + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&bars->ring_empty[s]);
+                    dRingMn + slot_off(qs) + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars->slot_empty[qs]);
       }
-      if (i + 1 < nsteps) issue_dp(i + 1);
+      if (i + 1 < nsteps) {
+        if (!mbar_wait(&bars->slot_full[slot_early(i + 1)], use_next, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_dp(i + 1);
+      }
     }
     if (!ok && leader) fail(SITE_BW_MMA);
     if (leader) tc_commit(&bars->acc_done);
@@ -633,10 +658,10 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int i = 0; i < nsteps; ++i) {
       const int qt = qt0 + i;
-      // this step's -lse2 and -D of the 128 query columns came with its Q and dO tiles
+      // this step's -lse2 and -D of the 128 query columns came with its dO tile
       const float* nl2v = vec + (i & 1) * 2 * C::BM + hf * 64;  // this half's 64 columns
       const float* ndv = nl2v + C::BM;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->ring_full[i & 1], (i >> 1) & 1, tmo, abort_flag) &&
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->slot_full[slot_early(i)], (i >> 1) & 1, tmo, abort_flag) &&
                                        mbar_wait(&bars->s_full, i & 1, tmo, abort_flag))) {
         ok = false;
         break;

@@ -31,26 +31,32 @@ namespace fa {
 // ---------------------------------------------------------------------------
 // Per query row, into the row-vector workspace [2][B*Hq][T_pad]: -D = -rowsum(dO * O)
 // (plane 0) and -lse * log2(e), the row's LSE in base 2 negated (plane 1; -inf for
-// a row with no visible key, so that its P is 0). One warp per row.
+// a row with no visible key, so that its P is 0). A group of d / 8 lanes takes a
+// row, one 16-byte load of O and of dO per lane (HBM-bound: every byte of O and dO
+// is read once).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) bwd_rowsum_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ d_o,
                                                          const float* __restrict__ lse, float* __restrict__ vecs,
                                                          long long rows, int T, int T_pad, int d) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(o + row * d);
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(d_o + row * d);
+  const int lanes = d / 8;  // 16 (d = 128) or 8 (d = 64): a power of two dividing 32
+  const int sub = threadIdx.x & (lanes - 1);
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / lanes;
   float acc = 0.f;
-  for (int c = lane; c < d / 2; c += 32) {
-    const float2 x = __bfloat1622float2(a[c]);
-    const float2 y = __bfloat1622float2(b[c]);
-    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-  }
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * d + sub * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(d_o + row * d + sub * 8);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(a2[k]);
+      const float2 y = __bfloat1622float2(g2[k]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+  }
+  for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) {
     const long long bh = row / T;
     const long long at = bh * T_pad + (row - bh * T);
     const long long plane = (rows / T) * T_pad;
@@ -864,7 +870,8 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
       return FA_ERR_CUDA;
   }
   const long long rows = static_cast<long long>(B) * Hq * T;
-  bwd_rowsum_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+  const long long rows_per_block = 256 / (d / 8);
+  bwd_rowsum_kernel<<<static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, vecs, rows, T, T_pad, d);
   BwParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);

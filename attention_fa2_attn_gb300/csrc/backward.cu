@@ -9,21 +9,26 @@
 // a KV head's dK, dV summing over the query heads of its group; masked scores
 // (bottom-right causal mask) have P = 0.
 //
-// How (GB300-specific): three launches.
-//   * bwd_rowsum_kernel: D, one warp per query row (HBM-bound, tiny).
-//   * bwd_dq_kernel: one 128-row query tile per CTA (a GQA group's heads stacked
-//     as rows, as in the forward) looping over 128-key tiles. tcgen05 MMAs put
-//     S = Q K^T and dP = dO V^T in TMEM; four warps (one row per thread) form
-//     dS = P * (dP - D) in bf16 over S's columns; dQ += dS K takes dS straight
-//     from TMEM as the A operand.
-//   * bwd_dkdv_kernel: one 128-key tile per CTA looping over the query tiles.
-//     S^T = K Q^T and dP^T = V dO^T in TMEM (rows = keys); the warps write P^T and
-//     dS^T in bf16 over them; dV += P^T dO and dK += dS^T Q read them from TMEM,
-//     with dO and Q as MN-major operands from shared memory. dK and dV
-//     accumulate in TMEM over all query tiles and all heads of the group.
-// Computing dQ in its own kernel (recomputing S and dP there) keeps every
-// accumulator in TMEM and needs no atomics. Each step runs the two MMA groups
-// and the elementwise pass in turn.
+// How (GB300-specific): two launches.
+//   * bwd_rowsum_kernel: per query row, -D and the negated base-2 LSE into a small
+//     workspace (HBM-bound, tiny).
+//   * bwd_kernel: the dK/dV pass and the dQ pass as the two halves of one grid,
+//     the dQ CTAs filling the last wave of the dK/dV ones.
+//     - dK/dV (bwd_dkdv_cta): one 128-key tile per CTA looping over the query tiles
+//       (a GQA group's heads stacked as rows, as in the forward). S^T = K Q^T and
+//       dP^T = V dO^T in TMEM (rows = keys); eight warps write P^T and dS^T in bf16
+//       over them; dV += P^T dO and dK += dS^T Q read them from TMEM, with dO and Q
+//       as MN-major operands from shared memory. dK and dV accumulate in TMEM over
+//       all query tiles and all heads of the group.
+//     - dQ (bwd_dq_cta): one 128-row query tile per CTA looping over 128-key tiles.
+//       S = Q K^T and dP = dO V^T in TMEM; the warps form dS = P * (dP - D) in bf16
+//       over dP's columns; dQ += dS K takes dS straight from TMEM as the A operand.
+//     The streamed tiles (Q and dO, or K and V) rotate through four shared-memory
+//     slots so that the tile needed first in step j + 2 loads as soon as the step
+//     j tile that is released early frees its slot.
+// Computing dQ in its own pass (recomputing S and dP there) keeps every
+// accumulator in TMEM and needs no atomics. MMAs of neighbouring tiles overlap
+// each tile's elementwise work.
 #include "common.cuh"
 
 namespace fa {
@@ -148,12 +153,12 @@ __device__ __forceinline__ int slot_late(int j) { return 2 * (j & 1) + ((j >> 1)
 __device__ __forceinline__ int slot_early(int j) { return 2 * (j & 1) + 1 - ((j >> 1) & 1); }
 
 // ---------------------------------------------------------------------------
-// dQ: one stacked query tile per CTA, looping over key tiles
+// dQ: one stacked query tile qt of (batch, KV head) bkv per CTA, looping over key tiles
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(320, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwParams p) {
+__device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmDO, const CUtensorMap& tmK,
+                                           const CUtensorMap& tmV, const BwParams& p, const int qt,
+                                           const int bkv) {
   using C = BwCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -163,8 +168,6 @@ __global__ void __launch_bounds__(320, 1)
   BwBars* bars = reinterpret_cast<BwBars*>(smem + C::OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
-  const int bkv = blockIdx.y;
   const int b = bkv / p.Hkv;
   const int kvh = bkv % p.Hkv;
   const int shift = p.S - p.T;
@@ -449,13 +452,14 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dK, dV: one 128-key tile per CTA, looping over the stacked query tiles
+// dK, dV: one 128-key tile kt of (batch, KV head) bkv per CTA, looping over the
+// stacked query tiles
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(320, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmVec, const BwParams p) {
+__device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUtensorMap& tmDO,
+                                             const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                             const CUtensorMap& tmVec, const BwParams& p, const int kt,
+                                             const int bkv) {
   using C = BwCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -466,8 +470,6 @@ __global__ void __launch_bounds__(320, 1)
   float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // per ring stage: [-lse2 | -D][128]
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kt = blockIdx.x;
-  const int bkv = blockIdx.y;
   const int b = bkv / p.Hkv;
   const int kvh = bkv % p.Hkv;
   const int shift = p.S - p.T;
@@ -798,6 +800,27 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Both passes in one launch: the first n_ktiles * B * Hkv CTAs compute dK/dV (heaviest
+// key tiles first under the causal mask), the rest dQ (heaviest query tiles first),
+// so the last wave of the first pass fills with work of the second. The two passes
+// share no data but the inputs.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmVec, const BwParams p) {
+  const int n_kv = p.n_ktiles * p.B * p.Hkv;
+  const int x = static_cast<int>(blockIdx.x);
+  if (x < n_kv) {
+    bwd_dkdv_cta<D>(tmQ, tmDO, tmK, tmV, tmVec, p, x % p.n_ktiles, x / p.n_ktiles);
+  } else {
+    const int y = x - n_kv;
+    bwd_dq_cta<D>(tmQ, tmDO, tmK, tmV, p, p.n_qtiles - 1 - y % p.n_qtiles, y / p.n_qtiles);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -830,14 +853,13 @@ template <int D>
 static int launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tvec, const BwParams& p, cudaStream_t stream) {
   using C = BwCfg<D>;
-  auto kq = bwd_dq_kernel<D>;
-  auto kkv = bwd_dkdv_kernel<D>;
-  if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess ||
-      cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+  auto kfn = bwd_kernel<D>;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
   const unsigned nbkv = static_cast<unsigned>(p.B * p.Hkv);
-  kkv<<<dim3(p.n_ktiles, nbkv), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, tvec, p);
-  kq<<<dim3(p.n_qtiles, nbkv), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, p);
+  const long long ctas = static_cast<long long>(p.n_ktiles + p.n_qtiles) * nbkv;
+  if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  kfn<<<static_cast<unsigned>(ctas), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, tvec, p);
   return launch_status();
 }
 

@@ -393,7 +393,7 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     ms = time_steps(torch, step, bsteps, stream)
     tf = cm.attention_backward_flops(w.B, w.Hq, w.T, w.S, w.d, w.causal) / (ms * 1e-3) / 1e12
     out["backward_" + w.name] = {"metric": "attn bwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
-                                 "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 3,
+                                 "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 2,
                                  "steps": bsteps,
                                  "flops": "2.5 x the forward's 4*T*S*d (S, dP, dV, dK, dQ); dQ's kernel recomputes S and dP"}
     del q, k, v, d_o, o, lse, ws, dq, dk, dv

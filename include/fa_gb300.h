@@ -111,8 +111,9 @@ FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, floa
  *   {1, 2, 4, 8, 16}.
  *   workspace: device scratch of at least fa_bwd_workspace_bytes(B, Hq, Tq)
  *   bytes, 16-byte aligned, for two fp32 values per query row: -D and the LSE in
- *   base 2, negated. Three launches on `stream`: those row values, then dK/dV
- *   (one CTA per 128-key tile), then dQ (one CTA per 128-row query tile).
+ *   base 2, negated. Two launches on `stream`: those row values, then one grid
+ *   whose first CTAs compute dK/dV (one per 128-key tile) and whose others
+ *   compute dQ (one per 128-row query tile).
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                         const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq,

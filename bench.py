@@ -524,18 +524,36 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
     peak = peaks["bf16_tflops"]
     traffic = load_traffic().get("prefill_tc_kernel")
 
-    # end to end: pinned host inputs -> HBM -> kernel -> O and lse back to pinned host memory
+    # end to end: pinned host inputs -> HBM -> kernel -> O and lse back to pinned host memory.
+    # The batch is pipelined over three streams: batch element b's inputs are copied in on
+    # s_in, its fa_fwd runs on the bench stream once they have landed, and its O and lse are
+    # copied out on s_out. So the copies of one element overlap the kernel of another.
+    # Each step starts after the previous step's kernels are done with the device buffers,
+    # and the bench stream waits for the last copy out.
     qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
     oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(w.B)]
+    ev_k = [torch.cuda.Event() for _ in range(w.B)]
 
     def e2e_step():
-        q.copy_(qh, non_blocking=True)
-        k.copy_(kh, non_blocking=True)
-        v.copy_(vh, non_blocking=True)
-        fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
+        s_in.wait_stream(stream)
+        for b in range(w.B):
+            with torch.cuda.stream(s_in):
+                q[b].copy_(qh[b], non_blocking=True)
+                k[b].copy_(kh[b], non_blocking=True)
+                v[b].copy_(vh[b], non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            fa.fa_fwd(q[b : b + 1], k[b : b + 1], v[b : b + 1], causal=w.causal, scale=w.scale, out=o[b : b + 1],
+                      lse=lse[b : b + 1])
+            ev_k[b].record(stream)
+            s_out.wait_event(ev_k[b])
+            with torch.cuda.stream(s_out):
+                oh[b].copy_(o[b], non_blocking=True)
+                lh[b].copy_(lse[b], non_blocking=True)
+        stream.wait_stream(s_out)
 
     for _ in range(2):
         e2e_step()

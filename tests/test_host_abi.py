@@ -133,3 +133,20 @@ def test_kv_outer_workspace_and_rejections(L):
     assert ko(Hq=3) == _lib.FA_ERR_INVALID_ARG
     assert ko(d=96, ws_bytes=1 << 30) == _lib.FA_ERR_UNSUPPORTED
     assert ko(Hq=12, Hkv=4, ws_bytes=1 << 30) == _lib.FA_ERR_UNSUPPORTED  # group of 3
+
+
+def test_bwd_workspace_and_rejections(L):
+    # two fp32 values per query row, rows padded to a multiple of 4 (16 bytes)
+    assert L.fa_bwd_workspace_bytes(2, 4, 301) == 2 * 2 * 4 * 304 * 4
+    assert L.fa_bwd_workspace_bytes(1, 1, 8) == 2 * 8 * 4
+    assert L.fa_bwd_workspace_bytes(0, 4, 8) == 0
+    need = L.fa_bwd_workspace_bytes(1, 2, 8)
+
+    def bwd(*, ws=P, ws_bytes=need, Hq=2, Hkv=2, d=128, lse=P):
+        return L.fa_bwd(P, P, P, P, lse, P, P, P, P, 1, Hq, Hkv, 8, 8, d, 0.1, 1, ws, ws_bytes, None)
+
+    assert bwd(ws_bytes=need - 1) == _lib.FA_ERR_INVALID_ARG
+    assert bwd(ws=None) == _lib.FA_ERR_INVALID_ARG
+    assert bwd(lse=None) == _lib.FA_ERR_INVALID_ARG
+    assert bwd(Hq=3) == _lib.FA_ERR_INVALID_ARG
+    assert bwd(d=96) == _lib.FA_ERR_UNSUPPORTED

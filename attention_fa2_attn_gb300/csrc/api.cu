@@ -211,8 +211,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const int g = Hq / Hkv;
   if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * Hq * Tq >= (1ll << 31) || static_cast<long long>(B) * Hkv * Skv >= (1ll << 31) ||
-      static_cast<long long>(B) * Hkv > 65535)
+  if (static_cast<long long>(B) * Hq * Tq >= (1ll << 31) || static_cast<long long>(B) * Hkv * Skv >= (1ll << 31))
     return FA_ERR_UNSUPPORTED;
   unsigned* err = error_word();
   if (!err) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));

@@ -47,6 +47,12 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
+# GB300 datasheet figures, reported beside the measured ones: dense bf16 tensor
+# throughput and HBM3e bandwidth
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+
+
 def load_traffic():
     """dram bytes per launch from the committed ncu summary, if it matches the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
@@ -298,7 +304,7 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     ms = time_steps(torch, step, steps, stream)
     tf = cm.attention_flops(w.B, w.Hq, w.T, w.S, w.d, True) / (ms * 1e-3) / 1e12
     out[w.name] = {"metric": "attn fwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
-                   "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 1}
+                   "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "frac_of_nominal_bf16": tf / NOMINAL_BF16_TFLOPS, "launches_per_step": 1}
     del q, k, v, o, lse
 
     # split-KV decode (decode kernel + merge)
@@ -318,7 +324,7 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     byt = cm.decode_bytes(w.B, w.Hq, w.Hkv, w.T, w.S, w.d)
     gbs = byt / (ms * 1e-3) / 1e9
     out[w.name] = {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
-                   "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "launches_per_step": 2,
+                   "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_hbm": gbs / NOMINAL_HBM_GBS, "launches_per_step": 2,
                    "bytes_per_step": byt, "num_splits": w.num_splits,
                    "traffic": load_traffic().get("decode_kernel_splitkv")}
     del q, k, v, o, lse, ws
@@ -344,7 +350,7 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     byt = cm.decode_bytes(w.B, w.Hq, w.Hkv, w.T, w.S, w.d, page_size=w.page_size)
     gbs = byt / (ms * 1e-3) / 1e9
     out[w.name] = {"metric": "decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": ms,
-                   "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "launches_per_step": 1,
+                   "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_hbm": gbs / NOMINAL_HBM_GBS, "launches_per_step": 1,
                    "bytes_per_step": byt, "num_splits": 1,
                    "traffic": load_traffic().get("decode_kernel_paged")}
     del q, kp, vp, table, sl, o, lse
@@ -370,7 +376,7 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     ms = time_steps(torch, step, steps, stream)
     tf = cm.chunked_attention_flops(w.Hq, w.T, seqlens, w.d, True) / (ms * 1e-3) / 1e12
     out[w.name] = {"metric": "attn fwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
-                   "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 1,
+                   "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "frac_of_nominal_bf16": tf / NOMINAL_BF16_TFLOPS, "launches_per_step": 1,
                    "flops": "4*d per visible (query, key) pair under the bottom-right mask",
                    "seqlens": list(seqlens)}
     del q, kp, vp, table, sl, o, lse
@@ -393,7 +399,7 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     ms = time_steps(torch, step, bsteps, stream)
     tf = cm.attention_backward_flops(w.B, w.Hq, w.T, w.S, w.d, w.causal) / (ms * 1e-3) / 1e12
     out["backward_" + w.name] = {"metric": "attn bwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
-                                 "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "launches_per_step": 2,
+                                 "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "frac_of_nominal_bf16": tf / NOMINAL_BF16_TFLOPS, "launches_per_step": 2,
                                  "steps": bsteps,
                                  "flops": "2.5 x the forward's 4*T*S*d (S, dP, dV, dK, dQ); dQ's kernel recomputes S and dP"}
     del q, k, v, d_o, o, lse, ws, dq, dk, dv
@@ -609,7 +615,8 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
                        "causal": w.causal, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (Q, K, V, O: 268 MB per step)"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic, "kernel": "prefill_tc_kernel<128>",
+                         "frac": achieved / peak, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                         "traffic": traffic, "kernel": "prefill_tc_kernel<128>",
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                          else "fallback 1.9 PFLOP/s bf16 burst"},
             "e2e": {"value": job_throughput(flops, world, ms_e2e) / 1e12, "unit": "TFLOP/s",

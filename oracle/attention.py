@@ -16,7 +16,7 @@ Sources (page title, section):
           backward pass saves", "GQA loads KV once per group", "The block-table
           cost of paged attention".
 
-Conventions (readings where the pages are silent; each is listed in the design doc):
+Conventions (readings where the pages are silent):
   * Layout: q, o are [B][Hq][T][d]; k, v are [B][Hkv][S][d] (per-(batch, head)
     planes of [rows][d], as the FA1 kernel indexes them).
   * Scores are x_j = scale * (q . k_j); lse is the natural log-sum-exp of the

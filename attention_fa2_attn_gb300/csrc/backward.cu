@@ -16,9 +16,11 @@
 //     the dQ CTAs filling the last wave of the dK/dV ones.
 //     - dK/dV (bwd_dkdv_cta): one 128-key tile per CTA looping over the query tiles
 //       (a GQA group's heads stacked as rows, as in the forward). S^T = K Q^T and
-//       dP^T = V dO^T in TMEM (rows = keys); eight warps write P^T and dS^T in bf16
-//       over them; dV += P^T dO and dK += dS^T Q read them from TMEM, with dO and Q
-//       as MN-major operands from shared memory. dK and dV accumulate in TMEM over
+//       dP^T = V dO^T in TMEM (rows = keys); eight warps write P^T in bf16 to a
+//       swizzled shared-memory tile (so S^T of the next tile can overwrite S^T as
+//       soon as it has been read) and dS^T in bf16 over dP^T's columns; dV += P^T dO
+//       reads P^T from shared memory, dK += dS^T Q reads dS^T from TMEM, with dO and
+//       Q as MN-major operands from shared memory. dK and dV accumulate in TMEM over
 //       all query tiles and all heads of the group.
 //     - dQ (bwd_dq_cta): one 128-row query tile per CTA looping over 128-key tiles.
 //       S = Q K^T and dP = dO V^T in TMEM; the warps form dS = P * (dP - D) in bf16
@@ -85,9 +87,14 @@ struct BwCfg {
   // smem: two fixed tiles (Q and dO, or K and V), then a ring of STAGES tile pairs
   static constexpr int OFF_FIX = 0;
   static constexpr int OFF_RING = 2 * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_RING + STAGES * 2 * TILE_BYTES;
+  // dK/dV: P^T of the current step in bf16 (128 keys x 128 queries, two 128-byte-swizzled
+  // chunks of 64 queries), the A operand of dV
+  static constexpr int OFF_PT = OFF_RING + STAGES * 2 * TILE_BYTES;
+  static constexpr int PT_BYTES = 128 * 128 * 2;
+  static constexpr int OFF_BAR = OFF_PT + PT_BYTES;
   static constexpr int OFF_VEC = OFF_BAR + 256;  // dK/dV: per ring stage, -lse2 and -D of the query columns
-  static constexpr int SMEM = OFF_VEC + 2 * 2 * BM * 4 + 1024;
+  // the dynamic shared memory is declared 1024-byte aligned (checked at run time): no slack
+  static constexpr int SMEM = OFF_VEC + 2 * 2 * BM * 4;
   // warps 0-7 elementwise: warp w takes TMEM lanes 32(w%4).. and column half w/4
   // (every element is independent, so a pair splits a row's columns with no
   // exchange); warp 8 producer, warp 9 MMA
@@ -104,6 +111,8 @@ struct BwCfg {
   // K-step kk sit at column packed_col(kk) of the S (or dP) region.
   static __device__ __forceinline__ uint32_t packed_col(int kk) { return 64 * (kk >> 2) + (kk & 3) * 8; }
 };
+
+static_assert(BwCfg<128>::SMEM <= 232448, "shared memory of the d = 128 backward");
 
 struct BwParams {
   const __nv_bfloat16* q;
@@ -128,7 +137,11 @@ struct BwBars {
   uint64_t fix_full;      // the fixed tile pair landed
   uint64_t s_full;        // S (or S^T) of this step is in TMEM
   uint64_t dp_full;       // dP (or dP^T) of this step is in TMEM
-  uint64_t e_first;       // dQ: S read out of TMEM; dK/dV: P^T written
+  uint64_t e_first;       // dQ: S read out of TMEM; dK/dV: P^T written (even steps)
+  uint64_t e_first_odd;   // dK/dV: P^T of odd steps (the warps may finish step i+1's P before
+                          // the MMA warp has seen step i's)
+  uint64_t s_read;        // dK/dV: S^T read out of TMEM (S^T of the next step may overwrite it)
+  uint64_t pt_free;       // dK/dV: dV has read P^T from shared memory
   uint64_t e_second;      // dS (or dS^T) written
   uint64_t acc_done;      // the last accumulation finished
   uint64_t slot_full[4];  // a streamed tile landed in ring slot t
@@ -160,8 +173,8 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
                                            const CUtensorMap& tmV, const BwParams& p, const int qt,
                                            const int bkv) {
   using C = BwCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   uint8_t* sQ = smem + C::OFF_FIX;
   uint8_t* sDO = sQ + C::TILE_BYTES;
   uint8_t* sRing = smem + C::OFF_RING;  // four tile slots (slot_late / slot_early) for K and V
@@ -461,13 +474,14 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
                                              const CUtensorMap& tmVec, const BwParams& p, const int kt,
                                              const int bkv) {
   using C = BwCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem + C::OFF_FIX;
   uint8_t* sV = sK + C::TILE_BYTES;
   uint8_t* sRing = smem + C::OFF_RING;  // four tile slots (slot_late / slot_early) for Q and dO
   BwBars* bars = reinterpret_cast<BwBars*>(smem + C::OFF_BAR);
   float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // per ring stage: [-lse2 | -D][128]
+  uint8_t* sPT = smem + C::OFF_PT;  // P^T of the current step, the A operand of dV
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int b = bkv / p.Hkv;
@@ -484,6 +498,9 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->e_first, C::EW_THREADS);
+    mbar_init(&bars->e_first_odd, C::EW_THREADS);
+    mbar_init(&bars->s_read, C::EW_THREADS);
+    mbar_init(&bars->pt_free, 1);
     mbar_init(&bars->e_second, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
     for (int t = 0; t < 4; ++t) {
@@ -564,11 +581,12 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     const uint64_t dRing = smem_desc_sw128(smem_u32(sRing), 16, 1024);               // Q (for S^T), dO (for dP^T)
     const uint64_t dRingMn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);  // Q (for dK), dO (for dV)
     auto slot_off = [](int t) { return static_cast<uint64_t>((t * C::TILE_BYTES) >> 4); };
-    // Issue order: S^T(0), dP^T(0), then per query tile n: dV(n) += P^T(n) dO_n (P^T
-    // over S^T's columns), S^T(n+1), dK(n) += dS^T(n) Q_n (dS^T over dP^T's),
-    // dP^T(n+1). Each overwrite comes after the MMA that reads the region in issue
-    // order; the warps' P phase of tile n+1 runs under dK(n) and dP^T(n+1), their
-    // dS phase under dV(n+1) and S^T(n+2). dV(n) gives dO_n's slot back, dK(n) Q_n's.
+    const uint64_t dPT = smem_desc_sw128(smem_u32(sPT), 16, 1024);  // P^T (keys x queries) as the A of dV
+    // Issue order: S^T(0), dP^T(0), then per query tile n: S^T(n+1) as soon as the warps
+    // have read S^T(n) out of TMEM, dV(n) += P^T(n) dO_n (P^T from shared memory),
+    // dK(n) += dS^T(n) Q_n (dS^T over dP^T's columns), dP^T(n+1). So S^T(n+1) runs under
+    // the warps' P phase of tile n, and dP^T(n+1) under their P phase of tile n+1. dV(n)
+    // gives dO_n's slot and the P^T buffer back, dK(n) Q_n's slot.
     auto issue_s = [&](int n) {
       const uint64_t so = slot_off(slot_late(n));
       if (leader) {
@@ -603,7 +621,16 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     }
     for (int i = 0; ok && i < nsteps; ++i) {
       const uint32_t use_next = ((i + 1) >> 1) & 1;  // slot parity of step i + 1
-      if (!mbar_wait(&bars->e_first, i & 1, tmo, abort_flag)) {
+      if (i + 1 < nsteps) {
+        if (!mbar_wait(&bars->s_read, i & 1, tmo, abort_flag) ||
+            !mbar_wait(&bars->slot_full[slot_late(i + 1)], use_next, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(i + 1);
+      }
+      if (!mbar_wait((i & 1) ? &bars->e_first_odd : &bars->e_first, (i >> 1) & 1, tmo, abort_flag)) {
         ok = false;
         break;
       }
@@ -611,19 +638,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
       if (leader) {
         const int ds = slot_early(i);
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_ts(tmem + C::COL_ACC, tmem + C::COL_S + C::packed_col(kk),
-                    dRingMn + slot_off(ds) + static_cast<uint64_t>((kk * 2048) >> 4), idesc_ts,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&bars->slot_empty[ds]);
-      }
-      if (i + 1 < nsteps) {
-        if (!mbar_wait(&bars->slot_full[slot_late(i + 1)], use_next, tmo, abort_flag)) {
-          ok = false;
-          break;
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          tc_mma_ss(tmem + C::COL_ACC, dPT + off, dRingMn + slot_off(ds) + static_cast<uint64_t>((kk * 2048) >> 4),
+                    idesc_ts, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_fence_after();
-        issue_s(i + 1);
+        tc_commit(&bars->slot_empty[ds]);
+        tc_commit(&bars->pt_free);
       }
       if (!mbar_wait(&bars->e_second, i & 1, tmo, abort_flag)) {
         ok = false;
@@ -681,13 +702,15 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
       const int vis_from = p.causal ? key - shift - qt * p.rows_per_head : INT_MIN;
       const bool masked = !__all_sync(0xffffffffu, key_valid && vis_from <= 0);
       // P phase: P^T = 2^(S^T*c - lse2[col]) for this half's 64 query columns, kept in
-      // registers and written (bf16) over this half's own S^T columns
+      // registers for the dS phase and written in bf16 to the shared-memory P^T tile
       float pv[64];
       {
         uint32_t sr[2][32];
         tmem_ld32(tS + hf * 64, sr[0]);
         tmem_ld32(tS + hf * 64 + 32, sr[1]);
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->s_read);  // S^T(i) is in registers: S^T(i+1) may overwrite it
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
@@ -710,16 +733,22 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
         for (int ii = 0; ii < 64; ++ii)
           if (!(key_valid && ((hf * 64 + ii) & rmask) >= vis_from)) pv[ii] = 0.f;
       }
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pp[16];
-#pragma unroll
-        for (int ii = 0; ii < 16; ++ii) pp[ii] = pack_bf16x2(pv[cc * 32 + 2 * ii], pv[cc * 32 + 2 * ii + 1]);
-        tmem_st16(tS + hf * 64 + cc * 16, pp);
+      // the P^T tile is free once dV(i-1) has read it
+      if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->pt_free, (i - 1) & 1, tmo, abort_flag))) {
+        ok = false;
+        break;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->e_first);
+      {
+        // row r (this key) of chunk hf: 8 16-byte units of 8 queries, 128-byte swizzle
+        uint8_t* prow = sPT + hf * C::CHUNK_BYTES + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) =
+              make_uint4(pack_bf16x2(pv[8 * u + 0], pv[8 * u + 1]), pack_bf16x2(pv[8 * u + 2], pv[8 * u + 3]),
+                         pack_bf16x2(pv[8 * u + 4], pv[8 * u + 5]), pack_bf16x2(pv[8 * u + 6], pv[8 * u + 7]));
+      }
+      fence_async_smem();  // the tensor core reads the tile through the async proxy
+      mbar_arrive((i & 1) ? &bars->e_first_odd : &bars->e_first);
       // dS phase: dS^T = P^T * (dP^T - D[col]) over this half's own dP^T columns
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, i & 1, tmo, abort_flag))) {
         ok = false;
@@ -810,6 +839,11 @@ __global__ void __launch_bounds__(320, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmVec, const BwParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment and the layout has no slack
+    if (threadIdx.x == 0) record_error(p.err, FA_ERR_BOUNDS, SITE_BW_SMEM);
+    return;
+  }
   const int n_kv = p.n_ktiles * p.B * p.Hkv;
   const int x = static_cast<int>(blockIdx.x);
   if (x < n_kv) {

@@ -32,6 +32,7 @@ enum ErrSite : unsigned {
   SITE_KO_PRODUCER = 12,
   SITE_KO_MMA = 13,
   SITE_KO_UPDATE = 14,
+  SITE_BW_SMEM = 15,
 };
 
 __device__ __forceinline__ void record_error(unsigned* err, unsigned code, unsigned site) {

@@ -26,7 +26,7 @@ int launch_decode(const void* q, const void* k, const void* v, const int* block_
                   int causal, int num_splits, void* workspace, cudaStream_t stream, unsigned* err,
                   unsigned long long timeout_ns);
 int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows, int d,
-                     cudaStream_t stream);
+                     cudaStream_t stream, bool after_split);
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
                     void* dq, void* dk, void* dv, float* vecs, int B, int Hq, int Hkv, int T, int S, int d,
                     float scale, int causal, cudaStream_t stream, unsigned* err, unsigned long long timeout_ns);
@@ -329,7 +329,8 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
                                static_cast<cudaStream_t>(stream), err, g_timeout_ns, nullptr, nullptr, 0, 0, n, o_part,
                                lse_part);
     if (rc == FA_OK && n > 1)
-      rc = launch_lse_merge(o_part, lse_part, o, lse, n, static_cast<int>(rows), d, static_cast<cudaStream_t>(stream));
+      rc = launch_lse_merge(o_part, lse_part, o, lse, n, static_cast<int>(rows), d, static_cast<cudaStream_t>(stream),
+                            true);
     if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
     return static_cast<fa_status>(rc);
   }
@@ -356,7 +357,7 @@ fa_status fa_lse_merge(const float* o_part, const float* lse_part, void* o, floa
   if (!o_part || !lse_part || !o) return FA_ERR_INVALID_ARG;
   if (num_splits < 1 || rows < 1 || d < 1) return FA_ERR_INVALID_ARG;
   if (d > 256) return FA_ERR_UNSUPPORTED;
-  int rc = launch_lse_merge(o_part, lse_part, o, lse, num_splits, rows, d, static_cast<cudaStream_t>(stream));
+  int rc = launch_lse_merge(o_part, lse_part, o, lse, num_splits, rows, d, static_cast<cudaStream_t>(stream), false);
   if (rc == FA_ERR_CUDA) cuda_fail(cudaGetLastError());
   return static_cast<fa_status>(rc);
 }

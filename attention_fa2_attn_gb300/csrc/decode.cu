@@ -494,8 +494,9 @@ EncodeTiledFn get_encode_tiled();
 template <bool PAGED>
 constexpr int dec_stages() { return PAGED ? 3 : 4; }
 
-// `after_split`: launched right behind the split kernel on the same stream, as a
-// programmatic dependent (its launch overlaps the split kernel's tail).
+// `after_split`: launched right behind the kernel that wrote the partials, on the
+// same stream, as a programmatic dependent (its launch overlaps that kernel's tail;
+// griddepcontrol.wait holds it until the partials are complete and visible).
 static int launch_lse_merge_impl(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows,
                                  int d, cudaStream_t stream, bool after_split) {
   const long long warps = static_cast<long long>(rows) * ((d + 31) / 32);
@@ -518,8 +519,8 @@ static int launch_lse_merge_impl(const float* o_part, const float* lse_part, voi
 }
 
 int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows, int d,
-                     cudaStream_t stream) {
-  return launch_lse_merge_impl(o_part, lse_part, o, lse, n, rows, d, stream, false);
+                     cudaStream_t stream, bool after_split) {
+  return launch_lse_merge_impl(o_part, lse_part, o, lse, n, rows, d, stream, after_split);
 }
 
 template <int D, bool PAGED>

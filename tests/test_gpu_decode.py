@@ -37,6 +37,10 @@ SPLIT_CASES = [
     (3, 4, 4, 1, 130, 64, False, 2),
     (1, 16, 2, 2, 300, 128, True, 64),  # more splits than 64-key tiles: empty splits
     (1, 4, 1, 3, 2, 128, True, 2),  # T > S: the first row sees no key
+    (1, 32, 8, 1, 4097, 128, True, 16),  # the split CTAs of a head merge in a 16-CTA cluster
+    (1, 32, 8, 1, 4097, 128, True, 17),  # too many splits for a cluster: merge launch
+    (2, 16, 1, 1, 3000, 64, False, 8),
+    (1, 16, 2, 1, 200, 128, True, 16),  # a 16-CTA cluster with empty splits
 ]
 
 
@@ -102,6 +106,7 @@ PAGED_CASES = [
     (4, 16, 2, 1, 64, [1000, 333, 64, 0], 64, 3),
     (2, 8, 1, 2, 128, [517, 260], 40, 1),
     (2, 64, 8, 1, 128, [2048, 1500], 128, 4),
+    (2, 64, 8, 1, 128, [2048, 9], 128, 16),  # 16-CTA clusters, one sequence mostly empty splits
 ]
 
 

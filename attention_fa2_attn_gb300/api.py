@@ -62,6 +62,16 @@ def fa_fwd_f32(q, k, v, causal: bool = False, scale: float | None = None):
     return o, lse
 
 
+def _ws_bytes(workspace, nbytes: int, device) -> int:
+    """Size in bytes of a caller's workspace tensor (any dtype), checked against what the call needs."""
+    if workspace.device != torch.device(device) or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    size = workspace.numel() * workspace.element_size()
+    if size < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes, got {size}")
+    return size
+
+
 def fa_bwd_workspace_bytes(B: int, Hq: int, T: int) -> int:
     return int(lib().fa_bwd_workspace_bytes(B, Hq, T))
 
@@ -79,13 +89,12 @@ def fa_bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = Non
     nbytes = fa_bwd_workspace_bytes(B, Hq, T)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    if workspace.numel() < nbytes:
-        raise ValueError(f"workspace needs {nbytes} bytes")
+    ws_bytes = _ws_bytes(workspace, nbytes, q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
-                      Hkv, T, S, d, scale, int(causal), _ptr(workspace), workspace.numel(), _stream(q))
+                      Hkv, T, S, d, scale, int(causal), _ptr(workspace), ws_bytes, _stream(q))
     check(st, "fa_bwd")
     return dq, dk, dv
 
@@ -106,12 +115,11 @@ def fa_fwd_kv_outer(q, k, v, causal: bool = False, scale: float | None = None, r
     nbytes = fa_fwd_kv_outer_workspace_bytes(B, Hq, T, d)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    if workspace.numel() < nbytes:
-        raise ValueError(f"workspace needs {nbytes} bytes")
+    ws_bytes = _ws_bytes(workspace, nbytes, q.device)
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
     st = lib().fa_fwd_kv_outer(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
-                               int(causal), int(row_bands), _ptr(workspace), workspace.numel(), _stream(q))
+                               int(causal), int(row_bands), _ptr(workspace), ws_bytes, _stream(q))
     check(st, "fa_fwd_kv_outer")
     return o, lse
 
@@ -145,9 +153,7 @@ def _workspace(B, Hq, T, d, n, device, workspace):
         return None, 0
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    if workspace.numel() < nbytes:
-        raise ValueError(f"workspace needs {nbytes} bytes")
-    return workspace, workspace.numel()
+    return workspace, _ws_bytes(workspace, nbytes, device)
 
 
 def fa_decode_splitkv(q, k, v, causal: bool = True, num_splits: int = 0, scale: float | None = None,

@@ -65,6 +65,21 @@ def test_splitkv_full_size():
     compare(o1, l1, o_ref, l_ref, what=w.name + " unsplit")
 
 
+@pytest.mark.parametrize("n,in_cluster", [(2, True), (16, True), (17, False)])
+def test_cluster_merge_and_merge_launch(n, in_cluster):
+    """One (batch, KV head): up to 16 split CTAs form one cluster and merge their
+    partials in shared memory, leaving the workspace as it was; 17 splits write the
+    partials to the workspace for the merge kernel. Both match the oracle."""
+    B, Hq, Hkv, T, S, d = 1, 4, 1, 1, 3000, 128
+    q, k, v = fi.qkv(B, Hq, Hkv, T, S, d, 91)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, 1.0 / math.sqrt(d), True)
+    fa = _fa()
+    ws = torch.full((fa.fa_decode_workspace_bytes(B, Hq, T, d, n) // 4,), float("nan"), device=DEV)
+    o, l = fa.fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, num_splits=n, workspace=ws)
+    compare(o, l, o_ref, l_ref, what=f"n={n}")
+    assert bool(torch.isnan(ws).all()) == in_cluster
+
+
 def test_merge_worked_example():
     """Partials of the scores [1, 2] | [3] with V = identity rows merge to the
     page's numbers: lse 3.408, weights 0.335 and 0.665."""

@@ -150,3 +150,16 @@ def test_bwd_workspace_and_rejections(L):
     assert bwd(lse=None) == _lib.FA_ERR_INVALID_ARG
     assert bwd(Hq=3) == _lib.FA_ERR_INVALID_ARG
     assert bwd(d=96) == _lib.FA_ERR_UNSUPPORTED
+
+
+def test_workspace_size_counts_bytes_of_any_dtype():
+    import torch
+
+    from attention_fa2_attn_gb300.api import _ws_bytes
+
+    assert _ws_bytes(torch.empty(10, dtype=torch.float32), 40, "cpu") == 40
+    assert _ws_bytes(torch.empty(40, dtype=torch.uint8), 40, "cpu") == 40
+    with pytest.raises(ValueError):
+        _ws_bytes(torch.empty(9, dtype=torch.float32), 40, "cpu")
+    with pytest.raises(ValueError):
+        _ws_bytes(torch.empty(20, dtype=torch.float32)[::2], 40, "cpu")

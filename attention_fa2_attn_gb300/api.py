@@ -17,11 +17,18 @@ from ._lib import FAError, check, lib
 
 
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # the C signatures declare c_void_p: a plain int address (or None for NULL) is passed as is
+    return None if t is None else t.data_ptr()
+
+
+# the current stream's raw handle, without building a torch Stream object per call
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(t: torch.Tensor):
-    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+    if _raw_stream is not None:
+        return _raw_stream(t.device.index)
+    return torch.cuda.current_stream(t.device).cuda_stream
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim: int):

@@ -520,13 +520,14 @@ __global__ void __launch_bounds__(160, PAGED ? 2 : 1)
 }
 
 // ---------------------------------------------------------------------------
-// LSE merge: one warp per (output row, 32-column slice)
+// LSE merge: one warp per output row
 // ---------------------------------------------------------------------------
-// lse = ln sum_s e^{lse_s};  O = sum_s e^{lse_s - lse} O_s. Each warp reduces the
-// row's lse over the splits itself (the lse_part reads are tiny and L2 resident);
-// the weights of 32 splits at a time sit one per lane and are broadcast by
-// shuffle, so a lane's loads of O_s for its column are independent of one
-// another and several are in flight at once.
+// lse = ln sum_s e^{lse_s};  O = sum_s e^{lse_s - lse} O_s. Lane s reads split s's
+// lse once (32 splits at a time) and the row's max, sum and weights come from warp
+// shuffles; the weight of split s is then broadcast from its lane while every lane
+// reads its NJ columns (col = lane + 32 j) of O_s. A row costs one round trip for
+// the lse values and one per G splits for the partials.
+template <int NJ, int G>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const float* __restrict__ o_part,
                                                         const float* __restrict__ lse_part,
                                                         __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
@@ -534,45 +535,61 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float* __restrict_
   // launched as a programmatic dependent of the split kernel: wait until that grid
   // has finished and its partials are visible (a no-op for a plain launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slices = (d + 31) >> 5;
-  const long long gw = static_cast<long long>(blockIdx.x) * 4 + warp;
-  if (gw >= static_cast<long long>(rows) * slices) return;
-  const int row = static_cast<int>(gw / slices);
-  const int col = static_cast<int>(gw % slices) * 32 + lane;
-  float mx = -INFINITY;
-  for (int s = lane; s < n; s += 32) mx = fmaxf(mx, lse_part[static_cast<size_t>(s) * rows + row]);
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const size_t step = static_cast<size_t>(rows) * d;  // one split's partials
+  const float ls0 = lane < n ? lse_part[static_cast<size_t>(lane) * rows + row] : -INFINITY;
+  float mx = ls0;
+  for (int s = 32 + lane; s < n; s += 32) mx = fmaxf(mx, lse_part[static_cast<size_t>(s) * rows + row]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   float tot = 0.f;
-  if (mx != -INFINITY)
-    for (int s = lane; s < n; s += 32) {
+  if (mx != -INFINITY) {
+    if (ls0 != -INFINITY) tot = expf(ls0 - mx);
+    for (int s = 32 + lane; s < n; s += 32) {
       const float ls = lse_part[static_cast<size_t>(s) * rows + row];
       if (ls != -INFINITY) tot += expf(ls - mx);
     }
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
   const float lrow = (mx == -INFINITY) ? -INFINITY : mx + logf(tot);
-  float acc = 0.f;
+  float acc[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) acc[j] = 0.f;
   if (mx != -INFINITY) {
     for (int s0 = 0; s0 < n; s0 += 32) {
-      float ws = 0.f;  // weight of split s0 + lane; 0 for an empty split (its O_s is never read)
-      if (s0 + lane < n) {
-        const float ls = lse_part[static_cast<size_t>(s0 + lane) * rows + row];
-        if (ls != -INFINITY) ws = expf(ls - lrow);
-      }
+      // weight of split s0 + lane; 0 for an empty split (its O_s is never read)
+      const float ls = s0 == 0 ? ls0 : (s0 + lane < n ? lse_part[static_cast<size_t>(s0 + lane) * rows + row] : -INFINITY);
+      const float ws = ls != -INFINITY ? expf(ls - lrow) : 0.f;
       const int cnt = min(32, n - s0);
-      const float* src = o_part + (static_cast<size_t>(s0) * rows + row) * d + col;
-      const size_t step = static_cast<size_t>(rows) * d;
-#pragma unroll 8
-      for (int i = 0; i < cnt; ++i) {
-        const float w = __shfl_sync(0xffffffffu, ws, i);
-        if (w != 0.f && col < d) acc = fmaf(w, src[i * step], acc);
+      const float* src = o_part + (static_cast<size_t>(s0) * rows + row) * d + lane;
+      // G splits' partials are loaded before any is used, so their loads overlap; an
+      // empty split's partial is read (it lies inside the buffer) but gets no weight
+      for (int g0 = 0; g0 < cnt; g0 += G) {
+        float v[G][NJ];
+#pragma unroll
+        for (int i = 0; i < G; ++i)
+#pragma unroll
+          for (int j = 0; j < NJ; ++j)
+            v[i][j] = (g0 + i < cnt && lane + 32 * j < d) ? src[(g0 + i) * step + 32 * j] : 0.f;
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const float w = __shfl_sync(0xffffffffu, ws, (g0 + i) & 31);
+          if (g0 + i < cnt && w != 0.f) {
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) acc[j] = fmaf(w, v[i][j], acc[j]);
+          }
+        }
       }
     }
   }
-  if (col < d) o[static_cast<size_t>(row) * d + col] = __float2bfloat16_rn(acc);
-  if (lse && gw % slices == 0 && lane == 0) lse[row] = lrow;
+  __nv_bfloat16* dst = o + static_cast<size_t>(row) * d + lane;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (lane + 32 * j < d) dst[32 * j] = __float2bfloat16_rn(acc[j]);
+  if (lse && lane == 0) lse[row] = lrow;
 }
 
 // ---------------------------------------------------------------------------
@@ -591,9 +608,8 @@ constexpr int dec_stages() { return PAGED ? 3 : 4; }
 // griddepcontrol.wait holds it until the partials are complete and visible).
 static int launch_lse_merge_impl(const float* o_part, const float* lse_part, void* o, float* lse, int n, int rows,
                                  int d, cudaStream_t stream, bool after_split) {
-  const long long warps = static_cast<long long>(rows) * ((d + 31) / 32);
-  if ((warps + 3) / 4 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  const int grid = static_cast<int>((warps + 3) / 4);
+  if (d < 1 || d > 256) return FA_ERR_UNSUPPORTED;
+  const int grid = static_cast<int>((static_cast<long long>(rows) + 3) / 4);  // one warp per row
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(128);
@@ -605,8 +621,24 @@ static int launch_lse_merge_impl(const float* o_part, const float* lse_part, voi
   cfg.attrs = attr;
   cfg.numAttrs = after_split ? 1 : 0;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
-  if (cudaLaunchKernelEx(&cfg, lse_merge_kernel, o_part, lse_part, ob, lse, n, rows, d) != cudaSuccess)
-    return FA_ERR_CUDA;
+  // loads in flight per lane: G splits x NJ columns. Many splits (decode) take the wider
+  // group; a few (the prefill key split, thousands of rows) the narrower one, which
+  // keeps more warps resident.
+  const bool wide = n >= 12;
+  cudaError_t e;
+  if (d <= 32)
+    e = wide ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<1, 8>, o_part, lse_part, ob, lse, n, rows, d)
+             : cudaLaunchKernelEx(&cfg, lse_merge_kernel<1, 4>, o_part, lse_part, ob, lse, n, rows, d);
+  else if (d <= 64)
+    e = wide ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<2, 8>, o_part, lse_part, ob, lse, n, rows, d)
+             : cudaLaunchKernelEx(&cfg, lse_merge_kernel<2, 4>, o_part, lse_part, ob, lse, n, rows, d);
+  else if (d <= 128)
+    e = wide ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<4, 8>, o_part, lse_part, ob, lse, n, rows, d)
+             : cudaLaunchKernelEx(&cfg, lse_merge_kernel<4, 4>, o_part, lse_part, ob, lse, n, rows, d);
+  else
+    e = wide ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<8, 4>, o_part, lse_part, ob, lse, n, rows, d)
+             : cudaLaunchKernelEx(&cfg, lse_merge_kernel<8, 2>, o_part, lse_part, ob, lse, n, rows, d);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
   return launch_status();
 }
 

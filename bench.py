@@ -473,6 +473,54 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
     out["prefill_one_head_sweep_b1_h1"] = {"metric": "attn fwd TFLOP/s", "unit": "TFLOP/s", "non_causal": True,
                                           "shapes": sweep}
     torch.cuda.empty_cache()
+
+    # the split heuristics swept over the batch: the split count each picks (num_splits = 0)
+    # against no split, for a one-head prefill and for a GQA decode step
+    hsweep = {"prefill_h1_n8192_d128": {}, "decode_hq32_hkv8_s16384_d128": {}}
+    for B in (1, 2, 4, 8):
+        N, d = 8192, 128
+        q, k, v = (rnd((B, 1, N, d), 1000 + 10 * B + i) for i in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, 1, N, device=dev)
+        n = fa.fa_num_splits_prefill(B, 1, 1, N, N, sms)
+        ws = torch.empty(max(1, fa.fa_decode_workspace_bytes(B, 1, N, d, n)), dtype=torch.uint8, device=dev)
+        flops = cm.attention_flops(B, 1, N, N, d, False)
+        res = {"num_splits": n}
+        for label, nn in (("auto", 0), ("unsplit", 1)):
+            step = lambda nn=nn: fa.fa_decode_splitkv(q, k, v, causal=False, num_splits=nn, workspace=ws,  # noqa: E731
+                                                      out=o, lse=lse)
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            ms = time_steps(torch, step, steps, stream)
+            res[label] = {"TFLOP/s": flops / (ms * 1e-3) / 1e12, "ms_per_step": ms}
+        hsweep["prefill_h1_n8192_d128"][f"B{B}"] = res
+        del q, k, v, o, lse, ws
+    for B in (1, 2, 4, 8, 16, 32):
+        Hq, Hkv, S, d = 32, 8, 16384, 128
+        q = rnd((B, Hq, 1, d), 1000 + B)
+        k = rnd((B, Hkv, S, d), 2000 + B)
+        v = rnd((B, Hkv, S, d), 3000 + B)
+        o = torch.empty_like(q)
+        lse = torch.empty(B, Hq, 1, device=dev)
+        n = fa.fa_num_splits_heuristic(B, Hkv, S, sms)
+        ws = torch.empty(max(1, fa.fa_decode_workspace_bytes(B, Hq, 1, d, n)), dtype=torch.uint8, device=dev)
+        byt = cm.decode_bytes(B, Hq, Hkv, 1, S, d)
+        res = {"num_splits": n}
+        for label, nn in (("auto", 0), ("unsplit", 1)):
+            step = lambda nn=nn: fa.fa_decode_splitkv(q, k, v, causal=True, num_splits=nn, workspace=ws,  # noqa: E731
+                                                      out=o, lse=lse)
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            ms = time_steps(torch, step, steps, stream)
+            res[label] = {"GB/s": byt / (ms * 1e-3) / 1e9, "ms_per_step": ms}
+        hsweep["decode_hq32_hkv8_s16384_d128"][f"B{B}"] = res
+        del q, k, v, o, lse, ws
+    out["split_heuristic_batch_sweep"] = {
+        "what": "num_splits = 0 (the heuristic's count) against 1, as the batch grows",
+        "prefill": "fa_num_splits_prefill, TFLOP/s", "decode": "fa_num_splits_heuristic, KV GB/s", **hsweep}
+    torch.cuda.empty_cache()
     return out
 
 

@@ -651,11 +651,19 @@ int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float*
 // their partials there without costing a wave: the clusters that fit on the GPU at
 // once (asked of the occupancy calculator, cached per split count) must cover the
 // grid in no more waves than the plain launch's CTAs would take.
+// The cache holds one answer per (device ordinal < 16, split count); concurrent host
+// threads can only write the same value into an entry.
 template <typename Kernel>
 static bool cluster_merge_fits(Kernel kfn, const cudaLaunchConfig_t& cfg, int nsplit, int nbh, int ctas_per_sm,
-                               int* active_cache) {
+                               int (*active_cache)[17]) {
   if (nsplit < 2 || nsplit > 16) return false;
-  int active = active_cache[nsplit];
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1 || dev < 0 || dev >= 16) {
+    cudaGetLastError();
+    return false;
+  }
+  int active = active_cache[dev][nsplit];
   if (active == 0) {
     active = -1;
     if (nsplit <= 8 || cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
@@ -663,15 +671,9 @@ static bool cluster_merge_fits(Kernel kfn, const cudaLaunchConfig_t& cfg, int ns
       if (cudaOccupancyMaxActiveClusters(&a, kfn, &cfg) == cudaSuccess && a > 0) active = a;
     }
     cudaGetLastError();  // a refused query is an answer, not an error of this call
-    active_cache[nsplit] = active;
+    active_cache[dev][nsplit] = active;
   }
   if (active < 1) return false;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      sms < 1) {
-    cudaGetLastError();
-    return false;
-  }
   const long long waves_cluster = (static_cast<long long>(nbh) + active - 1) / active;
   const long long slots = static_cast<long long>(sms) * ctas_per_sm;
   const long long waves_plain = (static_cast<long long>(nsplit) * nbh + slots - 1) / slots;
@@ -686,7 +688,7 @@ static int launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, DecPara
   constexpr int ST = dec_stages<PAGED>();
   using C = DecCfg<D, ST>;
   auto kfn = decode_kernel<D, ST, PAGED>;
-  static int active_cache[17] = {0};  // clusters resident at once, per split count (-1: none)
+  static int active_cache[16][17] = {};  // clusters resident at once, per device and split count (-1: none)
   *merged = false;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;

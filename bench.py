@@ -579,34 +579,41 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
     traffic = load_traffic().get("prefill_tc_kernel")
 
     # end to end: pinned host inputs -> HBM -> kernel -> O and lse back to pinned host memory.
-    # The batch is pipelined over three streams: batch element b's inputs are copied in on
+    # The batch is pipelined over three streams in chunks: a chunk's inputs are copied in on
     # s_in, its fa_fwd runs on the bench stream once they have landed, and its O and lse are
-    # copied out on s_out. So the copies of one element overlap the kernel of another.
-    # Each step starts after the previous step's kernels are done with the device buffers,
-    # and the bench stream waits for the last copy out.
+    # copied out on s_out. So the copies of one chunk overlap the kernel of another. A chunk
+    # is a whole batch element, except that the last element goes in two halves of its KV
+    # heads (with their query heads), which shortens the kernel + copy-out tail after the
+    # last input lands. Each step starts after the previous step's kernels are done with the
+    # device buffers, and the bench stream waits for the last copy out.
     qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
     oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(w.B)]
-    ev_k = [torch.cuda.Event() for _ in range(w.B)]
+    grp = w.Hq // w.Hkv
+    chunks = [(b, 0, w.Hkv) for b in range(w.B - 1)]  # (batch element, KV heads [kv0, kv1))
+    half = w.Hkv // 2
+    chunks += [(w.B - 1, 0, half), (w.B - 1, half, w.Hkv)] if half >= 1 else [(w.B - 1, 0, w.Hkv)]
+    ev_in = [torch.cuda.Event() for _ in chunks]
+    ev_k = [torch.cuda.Event() for _ in chunks]
 
     def e2e_step():
         s_in.wait_stream(stream)
-        for b in range(w.B):
+        for i, (b, kv0, kv1) in enumerate(chunks):
+            h0, h1 = kv0 * grp, kv1 * grp
             with torch.cuda.stream(s_in):
-                q[b].copy_(qh[b], non_blocking=True)
-                k[b].copy_(kh[b], non_blocking=True)
-                v[b].copy_(vh[b], non_blocking=True)
-                ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
-            fa.fa_fwd(q[b : b + 1], k[b : b + 1], v[b : b + 1], causal=w.causal, scale=w.scale, out=o[b : b + 1],
-                      lse=lse[b : b + 1])
-            ev_k[b].record(stream)
-            s_out.wait_event(ev_k[b])
+                q[b, h0:h1].copy_(qh[b, h0:h1], non_blocking=True)
+                k[b, kv0:kv1].copy_(kh[b, kv0:kv1], non_blocking=True)
+                v[b, kv0:kv1].copy_(vh[b, kv0:kv1], non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            fa.fa_fwd(q[b : b + 1, h0:h1], k[b : b + 1, kv0:kv1], v[b : b + 1, kv0:kv1], causal=w.causal,
+                      scale=w.scale, out=o[b : b + 1, h0:h1], lse=lse[b : b + 1, h0:h1])
+            ev_k[i].record(stream)
+            s_out.wait_event(ev_k[i])
             with torch.cuda.stream(s_out):
-                oh[b].copy_(o[b], non_blocking=True)
-                lh[b].copy_(lse[b], non_blocking=True)
+                oh[b, h0:h1].copy_(o[b, h0:h1], non_blocking=True)
+                lh[b, h0:h1].copy_(lse[b, h0:h1], non_blocking=True)
         stream.wait_stream(s_out)
 
     for _ in range(2):
@@ -668,7 +675,8 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                          else "fallback 1.9 PFLOP/s bf16 burst"},
             "e2e": {"value": job_throughput(flops, world, ms_e2e) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                    "chunks_per_step": len(chunks)},
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": args.steps,

@@ -1,8 +1,7 @@
 // common.cuh -- inline-PTX building blocks for the sm_103a kernels, written
 // from the PTX ISA: mbarriers with bounded waits, TMA tensor loads and stores
 // without multicast, tcgen05 TMEM allocation / MMA / loads / stores, fences,
-// the cluster barrier and distributed-shared-memory loads, and the device-side
-// error word.
+// and the device-side error word.
 #pragma once
 
 #include <cuda.h>
@@ -341,44 +340,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// ----------------------------------------------------------------------------
-// Thread-block clusters: rank, distributed shared memory, the cluster barrier.
-// A non-cluster launch is a cluster of one CTA, where these reduce to the CTA.
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA in the cluster arrives (release) and waits (acquire):
-// writes to a CTA's shared memory before it are visible to peers' reads after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// The shared::cluster address of the same shared-memory offset in CTA `rank`.
-__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
 }
 
 // Host side: the status of the launches just made -- FA_OK, or FA_ERR_CUDA with the

@@ -25,15 +25,6 @@
 // output and the four are merged through shared memory at the end. For paged
 // K/V, the producer warp fetches 32 block-table entries at a time (one per
 // lane) one batch ahead, and issues one TMA box per 16-token page.
-//
-// The merge of the split partials runs in the split kernel when the n split
-// CTAs of every (batch, KV head) can form one thread-block cluster and the
-// clusters fit on the GPU in no more waves than the plain grid (n <= 16; at
-// one CTA per SM the GPU holds 15 clusters of 8 but only 7 of 16): each CTA
-// leaves its partial in shared memory, and after a cluster barrier the CTAs
-// read one another's partials through distributed shared memory, each
-// writing a share of the final O and lse. Otherwise the partials go to
-// global memory and a dependent launch of the merge kernel follows.
 #include "common.cuh"
 
 namespace fa {
@@ -48,20 +39,14 @@ struct DecCfg {
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int THREADS = 160;     // 4 consumer warps + 1 producer warp
-  // after the last tile the ring holds the four warps' (O, m, l), then this
-  // split's normalised O (16 rows x D fp32) and lse (16) for the in-cluster merge
-  static constexpr int OFF_PART = 4 * 16 * D * 4 + 1024;
-  static constexpr int OFF_PART_LSE = OFF_PART + 16 * D * 4;
-  static_assert(OFF_PART_LSE + 16 * 4 <= OFF_BAR, "merge scratch must fit in the ring");
 };
 
 struct DecParams {
   const __nv_bfloat16* q;
   __nv_bfloat16* o;  // final output (num_splits == 1)
   float* lse;        // final lse, may be null (num_splits == 1)
-  float* o_part;     // [n][rows_total][D] (num_splits > 1, not merged in the cluster)
+  float* o_part;     // [n][rows_total][D] (num_splits > 1)
   float* lse_part;   // [n][rows_total]
-  int merge_in_cluster;  // the n split CTAs of a (batch, KV head) form one cluster
   const int* block_table;
   const int* seqlens;
   int B, Hq, Hkv, T, S;
@@ -99,66 +84,6 @@ __device__ __forceinline__ uint32_t sw_off(int row, int d, int chunk_bytes) {
   const int ch = d >> 6;
   const int piece = (d & 63) >> 3;
   return ch * chunk_bytes + row * 128 + ((piece ^ (row & 7)) << 4) + ((d & 7) << 1);
-}
-
-// The exact merge of the n split partials of one (batch, KV head), run by the n CTAs
-// of its cluster: lse = ln sum_s e^{lse_s}, O = sum_s e^{lse_s - lse} O_s. Output
-// element groups (a row, four columns) are dealt round-robin over the cluster's
-// CTAs; each reads the n partials' lse and four O values through distributed shared
-// memory. Empty splits (lse_s = -inf) get weight 0 and are not read.
-template <int D>
-__device__ __forceinline__ void merge_partials_in_cluster(const DecParams& p, const uint8_t* part_o,
-                                                          const uint8_t* part_lse, int b, int kvh) {
-  constexpr int MAXN = 16;
-  constexpr int V = D / 4;
-  const int n = p.num_splits;
-  const int rank = static_cast<int>(cluster_ctarank());
-  const uint32_t o_loc = smem_u32(part_o), l_loc = smem_u32(part_lse);
-  uint32_t o_peer[MAXN], l_peer[MAXN];
-#pragma unroll
-  for (int s = 0; s < MAXN; ++s) {
-    const uint32_t peer = static_cast<uint32_t>(s < n ? s : 0);
-    o_peer[s] = dsmem_addr(o_loc, peer);
-    l_peer[s] = dsmem_addr(l_loc, peer);
-  }
-  const int items = p.rows * V;
-  for (int it = static_cast<int>(threadIdx.x) * n + rank; it < items; it += static_cast<int>(blockDim.x) * n) {
-    const int r = it / V;
-    const int c4 = (it % V) * 4;
-    float ls[MAXN];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < MAXN; ++s) {
-      ls[s] = s < n ? ld_dsmem_f32(l_peer[s] + r * 4) : -INFINITY;
-      mx = fmaxf(mx, ls[s]);
-    }
-    float lrow = -INFINITY;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (mx != -INFINITY) {
-      float tot = 0.f;
-#pragma unroll
-      for (int s = 0; s < MAXN; ++s)
-        if (ls[s] != -INFINITY) tot += expf(ls[s] - mx);
-      lrow = mx + logf(tot);
-      float4 v[MAXN];
-#pragma unroll
-      for (int s = 0; s < MAXN; ++s)
-        if (ls[s] != -INFINITY) v[s] = ld_dsmem_f32x4(o_peer[s] + (r * D + c4) * 4);
-#pragma unroll
-      for (int s = 0; s < MAXN; ++s)
-        if (ls[s] != -INFINITY) {
-          const float w = expf(ls[s] - lrow);
-          acc.x = fmaf(w, v[s].x, acc.x);
-          acc.y = fmaf(w, v[s].y, acc.y);
-          acc.z = fmaf(w, v[s].z, acc.z);
-          acc.w = fmaf(w, v[s].w, acc.w);
-        }
-    }
-    const int h = kvh * p.g + r / p.T;
-    const size_t row_g = (static_cast<size_t>(b) * p.Hq + h) * p.T + (r % p.T);
-    *reinterpret_cast<uint2*>(p.o + row_g * D + c4) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-    if (p.lse && c4 == 0) p.lse[row_g] = lrow;
-  }
 }
 
 // Paged decode runs two CTAs per SM (3-stage ring, 96 KB each): with 16-token
@@ -487,15 +412,6 @@ __global__ void __launch_bounds__(160, PAGED ? 2 : 1)
             *reinterpret_cast<uint32_t*>(dst + cc) = pack_bf16x2(a0 * inv, a1 * inv);
           }
           if (p.lse && (t & 7) == 0) p.lse[row_g] = lse_v;
-        } else if (p.merge_in_cluster) {
-          // this split's partial stays in shared memory for the peers to read
-          float* dst = reinterpret_cast<float*>(smem + C::OFF_PART) + r * D + c0;
-          for (int cc = 0; cc < D / 8; ++cc) {
-            float a = 0.f;
-            for (int w = 0; w < 4; ++w) a += wO[(w * 16 + r) * D + c0 + cc] * scl[w];
-            dst[cc] = a * inv;
-          }
-          if ((t & 7) == 0) reinterpret_cast<float*>(smem + C::OFF_PART_LSE)[r] = lse_v;
         } else {
           const size_t rows_total = static_cast<size_t>(p.B) * p.Hq * p.T;
           float* dst = p.o_part + (static_cast<size_t>(split) * rows_total + row_g) * D + c0;
@@ -508,14 +424,6 @@ __global__ void __launch_bounds__(160, PAGED ? 2 : 1)
         }
       }
     }
-  }
-  if (p.merge_in_cluster) {
-    // every thread of every split CTA of this (batch, KV head) passes both cluster
-    // barriers: after the first, all partials are in shared memory; after the
-    // second, no peer reads them any more and the CTA may exit
-    cluster_sync_all();
-    merge_partials_in_cluster<D>(p, smem + C::OFF_PART, smem + C::OFF_PART_LSE, b, kvh);
-    cluster_sync_all();
   }
 }
 
@@ -647,68 +555,16 @@ int launch_lse_merge(const float* o_part, const float* lse_part, void* o, float*
   return launch_lse_merge_impl(o_part, lse_part, o, lse, n, rows, d, stream, after_split);
 }
 
-// Whether the n split CTAs of each (batch, KV head) can run as one cluster and merge
-// their partials there without costing a wave: the clusters that fit on the GPU at
-// once (asked of the occupancy calculator, cached per split count) must cover the
-// grid in no more waves than the plain launch's CTAs would take.
-// The cache holds one answer per (device ordinal < 16, split count); concurrent host
-// threads can only write the same value into an entry.
-template <typename Kernel>
-static bool cluster_merge_fits(Kernel kfn, const cudaLaunchConfig_t& cfg, int nsplit, int nbh, int ctas_per_sm,
-                               int (*active_cache)[17]) {
-  if (nsplit < 2 || nsplit > 16) return false;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      sms < 1 || dev < 0 || dev >= 16) {
-    cudaGetLastError();
-    return false;
-  }
-  int active = active_cache[dev][nsplit];
-  if (active == 0) {
-    active = -1;
-    if (nsplit <= 8 || cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-      int a = 0;
-      if (cudaOccupancyMaxActiveClusters(&a, kfn, &cfg) == cudaSuccess && a > 0) active = a;
-    }
-    cudaGetLastError();  // a refused query is an answer, not an error of this call
-    active_cache[dev][nsplit] = active;
-  }
-  if (active < 1) return false;
-  const long long waves_cluster = (static_cast<long long>(nbh) + active - 1) / active;
-  const long long slots = static_cast<long long>(sms) * ctas_per_sm;
-  const long long waves_plain = (static_cast<long long>(nsplit) * nbh + slots - 1) / slots;
-  return waves_cluster <= waves_plain;
-}
-
-// `*merged` tells whether the split CTAs merged their partials in their cluster
-// (then no merge launch follows and the partial buffers are not touched).
 template <int D, bool PAGED>
-static int launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, DecParams p, int nsplit, int nbh,
-                           cudaStream_t stream, bool* merged) {
+static int launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p, int nsplit, int nbh,
+                           cudaStream_t stream) {
   constexpr int ST = dec_stages<PAGED>();
   using C = DecCfg<D, ST>;
   auto kfn = decode_kernel<D, ST, PAGED>;
-  static int active_cache[16][17] = {};  // clusters resident at once, per device and split count (-1: none)
-  *merged = false;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nsplit, nbh);
-  cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = nsplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const bool cluster = cluster_merge_fits(kfn, cfg, nsplit, nbh, PAGED ? 2 : 1, active_cache);
-  cfg.numAttrs = cluster ? 1 : 0;
-  p.merge_in_cluster = cluster ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, kfn, tk, tv, p) != cudaSuccess) return FA_ERR_CUDA;
-  *merged = cluster;
+  dim3 grid(nsplit, nbh);
+  kfn<<<grid, C::THREADS, C::SMEM, stream>>>(tk, tv, p);
   return launch_status();
 }
 
@@ -750,7 +606,6 @@ int launch_decode(const void* q, const void* k, const void* v, const int* block_
   p.lse = lse;
   p.o_part = nullptr;
   p.lse_part = nullptr;
-  p.merge_in_cluster = 0;
   if (num_splits > 1) {
     p.o_part = static_cast<float*>(workspace);
     const size_t obytes = ((static_cast<size_t>(num_splits) * rows_total * d * 4 + 255) / 256) * 256;
@@ -774,14 +629,13 @@ int launch_decode(const void* q, const void* k, const void* v, const int* block_
   p.timeout_ns = timeout_ns;
   const int nbh = B * Hkv;
   int rc;
-  bool merged = false;
   if (d == 128)
-    rc = paged ? launch_decode_t<128, true>(tk, tv, p, num_splits, nbh, stream, &merged)
-               : launch_decode_t<128, false>(tk, tv, p, num_splits, nbh, stream, &merged);
+    rc = paged ? launch_decode_t<128, true>(tk, tv, p, num_splits, nbh, stream)
+               : launch_decode_t<128, false>(tk, tv, p, num_splits, nbh, stream);
   else
-    rc = paged ? launch_decode_t<64, true>(tk, tv, p, num_splits, nbh, stream, &merged)
-               : launch_decode_t<64, false>(tk, tv, p, num_splits, nbh, stream, &merged);
-  if (rc != FA_OK || num_splits == 1 || merged) return rc;
+    rc = paged ? launch_decode_t<64, true>(tk, tv, p, num_splits, nbh, stream)
+               : launch_decode_t<64, false>(tk, tv, p, num_splits, nbh, stream);
+  if (rc != FA_OK || num_splits == 1) return rc;
   return launch_lse_merge_impl(p.o_part, p.lse_part, o, lse, num_splits, static_cast<int>(rows_total), d, stream,
                                true);
 }

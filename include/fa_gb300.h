@@ -183,21 +183,16 @@ FA_API int fa_num_splits_prefill(int B, int Hq, int Hkv, int T, int S, int num_s
 /*
  * fa_decode_workspace_bytes -- bytes of `workspace` a split decode needs:
  * FP32 partial outputs [num_splits][B*Hq*T][d] followed (256-byte aligned) by
- * FP32 partial lse [num_splits][B*Hq*T]. 0 when num_splits <= 1. Required
- * for every split call, also when the splits end up merging in a cluster.
+ * FP32 partial lse [num_splits][B*Hq*T]. 0 when num_splits <= 1.
  */
 FA_API size_t fa_decode_workspace_bytes(int B, int Hq, int T, int d, int num_splits);
 
 /*
  * fa_decode_splitkv -- attention of T new queries over S contiguous cached
  * keys, split into num_splits contiguous key ranges of ceil(S / num_splits)
- * keys, each processed by its own CTA, then merged. When the split CTAs of
- * each (batch, KV head) can run as one thread-block cluster (2 to 16 splits)
- * without taking more waves than a plain launch, they merge their partials
- * through distributed shared memory before they exit and the workspace is
- * not touched; otherwise the partials go to the workspace and the merge
- * kernel of fa_lse_merge follows on the same stream. ("Attention kernel
- * chains", "The log-sum-exp merge" and "How many splits for decode".)
+ * keys, each processed by its own CTAs, then merged by fa_lse_merge on the
+ * same stream. ("Attention kernel chains", "The log-sum-exp merge" and "How
+ * many splits for decode".)
  *   q [B][Hq][T][d] bf16; k, v [B][Hkv][S][d] bf16; o [B][Hq][T][d] bf16 out;
  *   lse [B][Hq][T] fp32 out (may be NULL).
  *   d in {64, 128}.

@@ -552,7 +552,8 @@ __global__ void __launch_bounds__(384, 1)
       const bool row_valid = pos < p.T;
       const int vis_last = pos + shift;  // causal: last visible key of this row
       float m = -INFINITY;
-      float l = 0.f;
+      float l = 0.f;   // sum of the unrounded p: the lse's sum
+      float lc = 0.f;  // per tile, bf16(p_top) - p_top of its largest p, rescaled like l
 
       for (int j = 0; j < my_nj; ++j, ++cnt) {
         if (!wwait(&bars->s_full[t], cnt & 1)) {
@@ -591,6 +592,13 @@ __global__ void __launch_bounds__(384, 1)
         const float m_new = (m_tile > m + kRescaleSlack) ? m_tile : m;  // m = -inf: first visible key sets it
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = ex2_approx(m - m_use);  // 1 if the reference is kept; 0 while nothing was seen
+        // The tile's largest p, computed exactly as the loop below computes it for
+        // that key, and its rounding to the bf16 the P V product consumes. Against
+        // a stale reference the largest p is up to 2^kRescaleSlack, not exactly 1,
+        // so its bf16 rounding would leave a near-one-hot row's O off by 2^-9
+        // relative; O's normaliser l + lc counts that term as P V sees it.
+        const float p_top = ex2_approx(fmaf(mx, c, -m_use));
+        const float p_top_err = __bfloat162float(__float2bfloat16_rn(p_top)) - p_top;
         // p = 2^(s*c - m): packed FFMA, MUFU ex2, bf16 pairs stored over S, 32 columns at a time
         const float2 nm2 = make_float2(-m_use, -m_use);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -611,6 +619,7 @@ __global__ void __launch_bounds__(384, 1)
         const float2 a23 = fadd2(acc[2], acc[3]);
         const float2 at = fadd2(a01, a23);
         l = fmaf(l, alpha, at.x + at.y);
+        lc = fmaf(lc, alpha, p_top_err);
         m = m_new;
 
         // O is rescaled only when the max of some row of this warp rose; that
@@ -672,7 +681,7 @@ __global__ void __launch_bounds__(384, 1)
       const size_t row_index = (static_cast<size_t>(w.b) * p.Hq + h) * p.T + pos;
       __nv_bfloat16* orow = p.o + row_index * D;
       if (ok) {
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = l > 0.f ? 1.f / (l + lc) : 0.f;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];

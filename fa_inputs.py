@@ -132,3 +132,84 @@ def sample_rows(B, Hq, T, n: int, seed: int, tile: int = 128):
             for r in range(start, min(T, start + tile)):
                 rows.add((bb, hh, r))
     return sorted(rows)
+
+
+# Score levels, in log2 units, that the hot keys of successive 128-key tiles sit
+# at: rises both below and above the kernels' rescale slack of 8, so that a row's
+# reference max is sometimes kept (the largest p then exceeds 1) and sometimes
+# moved (O and the running sum rescaled by 2^(m_old - m_new)).
+CLIMB_STEPS = (0.0, 10.0, 5.0, 12.0, 3.0, 9.0, 7.0, 20.0, 1.0, 11.0, 6.0, 8.5, 2.0, 14.0, 4.0, 10.0, 7.5, 9.5)
+
+
+def climbing_levels(n_tiles: int, pattern: str = "rise", steps=CLIMB_STEPS) -> list:
+    """Per key tile, the level (log2 units) of that tile's hot keys.
+
+    ``rise``: cumulative ``steps``, so the maximum climbs on every tile.
+    ``rise_fall``: the same climb for the first half of the tiles, then back down.
+    """
+    lv, acc = [], 0.0
+    for t in range(n_tiles):
+        acc += steps[t % len(steps)]
+        lv.append(acc)
+    if pattern == "rise_fall":
+        half = (n_tiles + 1) // 2
+        lv = lv[:half] + [lv[2 * half - 1 - t] - 3.0 for t in range(half, n_tiles)]
+    elif pattern != "rise":
+        raise ValueError(pattern)
+    return lv
+
+
+def climbing_qkv(B, Hq, Hkv, T, S, d, index: int, scale: float, pattern: str = "rise", hot: int = 1,
+                 mixed_rows: bool = False, steps=CLIMB_STEPS, v_scale: float = 1.0, v_hot=None, tile: int = 128,
+                 dtype=torch.bfloat16):
+    """Inputs whose row maximum climbs tile by tile (the online softmax's rescale path).
+
+    Each (batch, KV head) gets a direction u ~ N(0, I_d). Query rows are
+    u + 0.05 N(0, I) (with ``mixed_rows``, rows at odd positions use -u instead,
+    so that, within a group of adjacent rows, some climb and some do not). In key
+    tile t, the first ``hot`` keys are u scaled so that scale * (u . k) equals
+    climbing_levels(...)[t] * ln 2 minus 0.7 per further hot key (several keys
+    share the weight), plus 0.1 N(0, I) noise; all other keys are N(0, 1).
+    Values are v_scale * N(0, 1); with ``v_hot`` set, the hot keys' value rows
+    are the constant v_hot instead. Seeds as in ``qkv``; u from 5000 + index.
+    """
+    g = _gen(2000 + index)
+    u = torch.randn(B, Hkv, 1, d, generator=_gen(5000 + index))
+    k = torch.randn(B, Hkv, S, d, generator=g)
+    v = v_scale * torch.randn(B, Hkv, S, d, generator=_gen(3000 + index))
+    n_tiles = -(-S // tile)
+    levels = climbing_levels(n_tiles, pattern, steps)
+    usq = (u * u).sum(-1, keepdim=True)  # [B][Hkv][1][1]
+    for t in range(n_tiles):
+        for j in range(min(hot, S - t * tile)):
+            r = t * tile + j
+            x = levels[t] * math.log(2.0) - 0.7 * j  # target scaled score (natural units)
+            k[:, :, r : r + 1, :] = u * (x / scale) / usq + 0.1 * k[:, :, r : r + 1, :]
+            if v_hot is not None:
+                v[:, :, r, :] = v_hot
+    sign = torch.ones(T, 1)
+    if mixed_rows:
+        sign[1::2] = -1.0
+    qn = torch.randn(B, Hq, T, d, generator=_gen(1000 + index))
+    q = u.repeat_interleave(Hq // Hkv, dim=1) * sign + 0.05 * qn
+    return q.contiguous().to(dtype), k.to(dtype), v.to(dtype)
+
+
+def pages_from_contiguous(k, v, page_size: int, index: int):
+    """Lay contiguous K and V [B][Hkv][S][d] out as pools [P][page_size][Hkv][d]
+    scattered by one seeded random-permutation block table [B][ceil(S/page_size)]
+    (pool slots past S are zero). Returns (k_pool, v_pool, table)."""
+    B, Hkv, S, d = k.shape
+    max_pages = -(-S // page_size)
+    P = B * max_pages
+    perm = torch.randperm(P, generator=_gen(4000 + index))
+    table = perm.view(B, max_pages).to(torch.int32)
+    pools = []
+    for x in (k, v):
+        pool = torch.zeros(P, page_size, Hkv, d, dtype=x.dtype)
+        for b in range(B):
+            for p in range(max_pages):
+                rows = x[b, :, p * page_size : min(S, (p + 1) * page_size), :]  # [Hkv][n][d]
+                pool[int(table[b, p]), : rows.shape[1]] = rows.transpose(0, 1)
+        pools.append(pool)
+    return pools[0], pools[1], table

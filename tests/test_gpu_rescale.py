@@ -1,0 +1,127 @@
+"""The online softmax's rescale path under inputs whose row maximum keeps climbing.
+
+"Attention kernel chains", "The online softmax on numbers" rescales the running
+sum and output by alpha = e^(m_old - m_new) each time the maximum rises;
+"Softmax and FlashAttention", "Maths" shows why any common reference works. The
+prefill kernel moves its reference only when a tile's maximum climbs more than
+8 (log2 units) above it, so with N(0, 1) inputs that path almost never runs. The
+inputs here (``fa_inputs.climbing_qkv``) put hot keys in every 128-key tile at
+levels that climb by steps both below and above that slack, so the reference is
+sometimes kept (the largest p then exceeds 1) and sometimes moved (O rescaled in
+tensor memory). With ``mixed_rows`` adjacent rows disagree: some climb, some do
+not. Every comparison is element by element against the fp64 oracle at the
+standard bf16 bounds (O max 1e-2, mean 1e-3, lse 1e-3).
+
+Values are drawn 0.5 * N(0, 1) in the coverage cases: the rows are nearly one-hot,
+so O is close to single value rows, and the bf16 rounding of O itself (unit
+roundoff 2^-8) would otherwise take most of the absolute mean bound.
+"""
+
+import math
+
+import pytest
+import torch
+
+import fa_inputs as fi
+import oracle
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def _fa():
+    import attention_fa2_attn_gb300 as fa
+
+    return fa
+
+
+# Steps (log2 units) of the hot keys' level from tile to tile: the first tile sets
+# the reference high above the N(0, 1) keys; the last step stays under the slack.
+STALE_STEPS = {"stale_last": (30.0, 10.0, 3.3), "stale_three": (30.0, 5.0, 6.0, 2.5)}
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("steps", sorted(STALE_STEPS))
+def test_stale_reference_top_term(d, steps):
+    """One hot key per tile, all hot keys with the same value row 3.875 (exact in
+    bf16), ordinary keys weighing ~2^-30: the exact O is 3.875 in every element.
+    The last tile's hot key sits under the slack, so its p is 2^(0..8), not 1, and
+    is rounded to bf16 for the P V product. O's normaliser must count that term as
+    rounded, or O comes out up to 2^-8 relative off (0.0156 here)."""
+    st = STALE_STEPS[steps]
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = fi.climbing_qkv(1, 2, 2, 256, 128 * len(st), d, 210, scale, hot=1, steps=st, v_hot=3.875)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, False)
+    fa = _fa()
+    o, l = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=False, scale=scale)
+    compare(o, l, o_ref, l_ref, what=f"fa_fwd {steps} d{d}")
+    # the same through the key split (one range per tile: each partial ends stale)
+    o2, l2 = fa.fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=False, num_splits=len(st), scale=scale)
+    compare(o2, l2, o_ref, l_ref, what=f"split {steps} d{d}")
+
+
+CASES = [
+    # B, Hq, Hkv, T, S, d, causal, pattern, hot, mixed_rows
+    (1, 2, 2, 256, 2048, 64, False, "rise", 1, False),
+    (1, 2, 2, 256, 2048, 128, False, "rise", 2, True),
+    (1, 8, 1, 40, 2304, 128, True, "rise", 3, True),  # group 8: 16 positions x 8 heads per tile
+    (1, 16, 2, 64, 2304, 64, True, "rise_fall", 1, True),
+    (2, 4, 4, 300, 2200, 128, True, "rise_fall", 2, False),  # ragged last query and key tiles
+    (1, 4, 1, 200, 2100, 64, False, "rise", 2, True),  # group 4
+]
+
+
+def _ids(c):
+    return "B{}_Hq{}_Hkv{}_T{}_S{}_d{}_{}_{}_hot{}{}".format(*c[:6], "causal" if c[6] else "full", c[7], c[8],
+                                                             "_mixed" if c[9] else "")
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_climbing_max_prefill(case):
+    """At least 16 key tiles, both query tiles of a pair, the maximum rising on
+    every tile (or rising then falling), against the three-pass definition."""
+    B, Hq, Hkv, T, S, d, causal, pattern, hot, mixed = case
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = fi.climbing_qkv(B, Hq, Hkv, T, S, d, 220 + T % 11, scale, pattern=pattern, hot=hot,
+                              mixed_rows=mixed, v_scale=0.5)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, causal)
+    o, l = _fa().fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale)
+    compare(o, l, o_ref, l_ref, what=_ids(case))
+
+
+@pytest.mark.parametrize("d,causal,n", [(64, False, 3), (128, True, 5)])
+def test_climbing_max_key_split(d, causal, n):
+    """The key-split instantiation: each range restarts the running state, then the
+    LSE merge combines the partials."""
+    B, Hq, Hkv, T, S = 1, 2, 2, 256, 2304
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = fi.climbing_qkv(B, Hq, Hkv, T, S, d, 230 + n, scale, pattern="rise", hot=2, mixed_rows=True,
+                              v_scale=0.5)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, causal)
+    o, l = _fa().fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, num_splits=n, scale=scale)
+    compare(o, l, o_ref, l_ref, what=f"split d{d} n{n}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_climbing_max_paged(d):
+    """The paged instantiation (more than 16 stacked rows per KV head through
+    fa_decode_paged): climbing K/V scattered over 16-token pages, ragged sequence
+    lengths, bottom-right causal mask."""
+    B, Hq, Hkv, T, S = 2, 16, 2, 40, 2304
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = fi.climbing_qkv(B, Hq, Hkv, T, S, d, 240 + d, scale, pattern="rise_fall", hot=2, mixed_rows=True,
+                              v_scale=0.5)
+    kp, vp, table = fi.pages_from_contiguous(k, v, 16, 240 + d)
+    seqlens = torch.tensor([S, 1800], dtype=torch.int32)
+    o_ref, l_ref = oracle.decode_paged(q, kp, vp, table, seqlens, 16, scale, True)
+    o, l = _fa().fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), seqlens.to(DEV), causal=True,
+                                 scale=scale)
+    compare(o, l, o_ref, l_ref, what=f"paged d{d}")

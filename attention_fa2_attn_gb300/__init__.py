@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     FAError,
     fa_bwd,
     fa_bwd_workspace_bytes,
+    fa_decode_num_splits,
     fa_decode_paged,
     fa_decode_splitkv,
     fa_decode_splitkv_static,
@@ -18,6 +19,7 @@ from .api import (  # noqa: F401
     fa_fwd_kv_outer,
     fa_fwd_kv_outer_workspace_bytes,
     fa_get_last_device_error,
+    fa_get_wait_timeouts,
     fa_lse_merge,
     fa_num_splits_heuristic,
     fa_num_splits_prefill,

@@ -41,6 +41,7 @@ SIGNATURES = {
     "fa_fwd_kv_outer_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_num_splits_heuristic": (_I, [_I, _I, _I, _I]),
     "fa_num_splits_prefill": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "fa_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "fa_decode_splitkv_static": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
@@ -51,6 +52,7 @@ SIGNATURES = {
     ),
     "fa_get_last_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "fa_set_wait_timeout_ns": (None, [_ULL]),
+    "fa_get_wait_timeouts": (None, [ctypes.POINTER(_ULL), ctypes.POINTER(_ULL)]),
     "fa_selftest_wait_timeout": (_I, [_ULL, _P]),
 }
 

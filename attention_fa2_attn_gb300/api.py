@@ -143,15 +143,13 @@ def fa_num_splits_prefill(B: int, Hq: int, Hkv: int, T: int, S: int, num_sms: in
     return int(lib().fa_num_splits_prefill(B, Hq, Hkv, T, S, num_sms))
 
 
-def _resolve_splits(num_splits: int, B: int, Hq: int, Hkv: int, T: int, S: int, device, paged: bool = False) -> int:
-    if num_splits:
-        return int(num_splits)
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    if (Hq // Hkv) * T > 16:
-        # more than 16 stacked query rows run on the prefill kernel; it splits the
-        # keys only when its query tiles do not fill the GPU (contiguous K/V)
-        return 1 if paged else fa_num_splits_prefill(B, Hq, Hkv, T, S, sms)
-    return fa_num_splits_heuristic(B, Hkv, S, sms)
+def fa_decode_num_splits(B: int, Hq: int, Hkv: int, T: int, S: int, paged: bool = False,
+                         num_sms: int | None = None, device=None) -> int:
+    """The split count the decode calls take for num_splits = 0 (chosen by the C library)."""
+    if num_sms is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return int(lib().fa_decode_num_splits(B, Hq, Hkv, T, S, int(paged), int(num_sms)))
 
 
 def _workspace(B, Hq, T, d, n, device, workspace):
@@ -171,13 +169,14 @@ def fa_decode_splitkv(q, k, v, causal: bool = True, num_splits: int = 0, scale: 
     B, Hq, T, d = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    n = _resolve_splits(num_splits, B, Hq, Hkv, T, S, q.device)
+    # the workspace is sized for the count the library takes; num_splits passes through as given
+    n = int(num_splits) or fa_decode_num_splits(B, Hq, Hkv, T, S, False, device=q.device)
     ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
     o = torch.empty_like(q) if out is None else out
     if lse is None:
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
     st = lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
-                                 int(causal), n, _ptr(ws), ws_bytes, _stream(q))
+                                 int(causal), int(num_splits), _ptr(ws), ws_bytes, _stream(q))
     check(st, "fa_decode_splitkv")
     return o, lse
 
@@ -214,7 +213,7 @@ def fa_lse_merge(o_part, lse_part):
     return o, lse
 
 
-def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = True, num_splits: int = 1,
+def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = True, num_splits: int = 0,
                     scale: float | None = None, workspace=None, out=None, lse=None):
     """Paged decode: pools [P][16][Hkv][d] bf16, block_table [B][max_pages] int32, seqlens [B] int32."""
     _need(q, "q", torch.bfloat16, 4)
@@ -226,14 +225,14 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = Tr
     P, page_size, Hkv, _ = k_pages.shape
     max_pages = block_table.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    n = _resolve_splits(num_splits, B, Hq, Hkv, T, max_pages * page_size, q.device, paged=True)
+    n = int(num_splits) or fa_decode_num_splits(B, Hq, Hkv, T, max_pages * page_size, True, device=q.device)
     ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
     o = torch.empty_like(q) if out is None else out
     if lse is None:
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
     st = lib().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), _ptr(o),
-                               _ptr(lse), B, Hq, Hkv, T, max_pages, page_size, P, d, scale, int(causal), n, _ptr(ws),
-                               ws_bytes, _stream(q))
+                               _ptr(lse), B, Hq, Hkv, T, max_pages, page_size, P, d, scale, int(causal),
+                               int(num_splits), _ptr(ws), ws_bytes, _stream(q))
     check(st, "fa_decode_paged")
     return o, lse
 
@@ -250,6 +249,13 @@ def fa_set_wait_timeout_ns(ns: int) -> None:
     lib().fa_set_wait_timeout_ns(int(ns))
 
 
+def fa_get_wait_timeouts() -> tuple[int, int]:
+    """(bound of the waits between roles, bound of the waits before a CTA exits), in ns."""
+    w, u = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    lib().fa_get_wait_timeouts(ctypes.byref(w), ctypes.byref(u))
+    return int(w.value), int(u.value)
+
+
 def fa_selftest_wait_timeout(timeout_ns: int, device=None) -> None:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     st = lib().fa_selftest_wait_timeout(int(timeout_ns), ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
@@ -264,6 +270,7 @@ __all__ = [
     "fa_bwd_workspace_bytes",
     "fa_num_splits_heuristic",
     "fa_num_splits_prefill",
+    "fa_decode_num_splits",
     "fa_decode_workspace_bytes",
     "fa_decode_splitkv",
     "fa_decode_splitkv_static",
@@ -271,5 +278,6 @@ __all__ = [
     "fa_decode_paged",
     "fa_get_last_device_error",
     "fa_set_wait_timeout_ns",
+    "fa_get_wait_timeouts",
     "fa_selftest_wait_timeout",
 ]

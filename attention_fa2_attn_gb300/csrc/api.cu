@@ -40,6 +40,9 @@ __device__ unsigned g_fa_device_error;
 
 static thread_local char g_cuda_err[256] = "no error";
 static unsigned long long g_timeout_ns = 4000000000ull;
+// The settable wait bound never goes below this: a shorter one would report
+// timeouts that are not faults whenever the GPU is time-sliced with other work.
+static constexpr unsigned long long kMinWaitTimeoutNs = 1000000ull;  // 1 ms
 
 // Keeps the text of a CUDA error for fa_last_cuda_error_string; cudaSuccess (the
 // error was already consumed and recorded where it happened) keeps the old text.
@@ -136,7 +139,12 @@ const char* fa_status_string(int status) {
 
 const char* fa_last_cuda_error_string(void) { return g_cuda_err; }
 
-void fa_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns > 0 ? ns : 1; }
+void fa_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns < kMinWaitTimeoutNs ? kMinWaitTimeoutNs : ns; }
+
+void fa_get_wait_timeouts(unsigned long long* wait_ns, unsigned long long* unwind_ns) {
+  if (wait_ns) *wait_ns = g_timeout_ns;
+  if (unwind_ns) *unwind_ns = unwind_timeout(g_timeout_ns);
+}
 
 int fa_num_splits_heuristic(int B, int Hkv, int S, int num_sms) {
   if (B <= 0 || Hkv <= 0 || S <= 0 || num_sms <= 0) return 1;
@@ -162,6 +170,18 @@ int fa_num_splits_prefill(int B, int Hq, int Hkv, int T, int S, int num_sms) {
   if (n > cap) n = cap;
   if (n > 64) n = 64;
   return n < 1 ? 1 : static_cast<int>(n);
+}
+
+// More than 16 stacked query rows per KV head (g * T > 16: chunked prefill or a
+// multi-token decode step) go to the tensor-core prefill kernel, which tiles the
+// queries itself; a key split is then only for shapes with too few query tiles to
+// fill the GPU (contiguous K/V).
+static bool many_rows(int Hq, int Hkv, int T) { return static_cast<long long>(Hq / Hkv) * T > 16; }
+
+int fa_decode_num_splits(int B, int Hq, int Hkv, int T, int S, int paged, int num_sms) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || S < 1 || num_sms < 1 || Hq % Hkv != 0) return 1;
+  if (many_rows(Hq, Hkv, T)) return paged ? 1 : fa_num_splits_prefill(B, Hq, Hkv, T, S, num_sms);
+  return fa_num_splits_heuristic(B, Hkv, S, num_sms);
 }
 
 size_t fa_decode_workspace_bytes(int B, int Hq, int T, int d, int num_splits) {
@@ -274,12 +294,6 @@ static fa_status check_decode_common(const void* q, const void* o, int B, int Hq
   return FA_OK;
 }
 
-// More than 16 stacked query rows per KV head (g * T > 16: chunked prefill or a
-// multi-token decode step) go to the tensor-core prefill kernel, which tiles the
-// queries itself; a key split is then only for shapes with too few query tiles to
-// fill the GPU (contiguous K/V).
-static bool many_rows(int Hq, int Hkv, int T) { return static_cast<long long>(Hq / Hkv) * T > 16; }
-
 static fa_status check_many_rows(int Hq, int Hkv, int num_splits, bool paged) {
   const int g = Hq / Hkv;
   if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return FA_ERR_UNSUPPORTED;
@@ -310,7 +324,7 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
       // heuristic, limited to what the given workspace holds (none: no split)
       const int sms = sm_count();
       if (!sms) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
-      n = splits_that_fit(B, Hq, T, d, fa_num_splits_prefill(B, Hq, Hkv, T, S, sms), workspace, ws_bytes);
+      n = splits_that_fit(B, Hq, T, d, fa_decode_num_splits(B, Hq, Hkv, T, S, 0, sms), workspace, ws_bytes);
     } else if (n > 1) {
       if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
       if (ws_bytes < fa_decode_workspace_bytes(B, Hq, T, d, n)) return FA_ERR_INVALID_ARG;
@@ -338,7 +352,7 @@ fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, void* o
   if (n == 0) {
     const int sms = sm_count();
     if (!sms) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
-    n = fa_num_splits_heuristic(B, Hkv, S, sms);
+    n = fa_decode_num_splits(B, Hq, Hkv, T, S, 0, sms);
   }
   if (n > 1) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
@@ -391,7 +405,7 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
   if (n == 0) {
     const int sms = sm_count();
     if (!sms) return static_cast<fa_status>(cuda_fail(cudaGetLastError()));
-    n = fa_num_splits_heuristic(B, Hkv, max_pages * page_size, sms);
+    n = fa_decode_num_splits(B, Hq, Hkv, T, max_pages * page_size, 1, sms);
   }
   if (n > 1) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;

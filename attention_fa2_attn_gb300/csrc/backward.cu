@@ -209,6 +209,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
   const uint64_t tmo = p.timeout_ns;
+  const uint64_t tmo_unwind = unwind_timeout(tmo);  // copies landing, MMAs draining
   auto fail = [&](unsigned site) {
     record_error(p.err, FA_ERR_TIMEOUT, site);
     *abort_flag = 1;
@@ -249,12 +250,12 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
       }
       if (*abort_flag) {
         // copies in flight must land before the CTA exits
-        mbar_wait(&bars->fix_full, 0, tmo);
+        mbar_wait(&bars->fix_full, 0, tmo_unwind);
         for (int x = max(0, issued - 2); x < issued; ++x) {
-          mbar_wait(&bars->slot_full[slot_late(x)], (x >> 1) & 1, tmo);
-          mbar_wait(&bars->slot_full[slot_early(x)], (x >> 1) & 1, tmo);
+          mbar_wait(&bars->slot_full[slot_late(x)], (x >> 1) & 1, tmo_unwind);
+          mbar_wait(&bars->slot_full[slot_early(x)], (x >> 1) & 1, tmo_unwind);
         }
-        if (k_only >= 0) mbar_wait(&bars->slot_full[slot_late(k_only)], (k_only >> 1) & 1, tmo);
+        if (k_only >= 0) mbar_wait(&bars->slot_full[slot_late(k_only)], (k_only >> 1) & 1, tmo_unwind);
       }
     }
   } else if (warp == C::MMA_WARP) {
@@ -342,7 +343,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     }
     if (!ok && leader) fail(SITE_BW_MMA);
     if (leader) tc_commit(&bars->acc_done);
-    mbar_wait(&bars->acc_done, 0, tmo);
+    mbar_wait(&bars->acc_done, 0, tmo_unwind);
   } else {
     // ---- elementwise warps: one query row per thread pair (TMEM lane), column half hf
     const int r = threadIdx.x & 127;
@@ -516,6 +517,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
   const uint64_t tmo = p.timeout_ns;
+  const uint64_t tmo_unwind = unwind_timeout(tmo);  // copies landing, MMAs draining
   auto fail = [&](unsigned site) {
     record_error(p.err, FA_ERR_TIMEOUT, site);
     *abort_flag = 1;
@@ -564,12 +566,12 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
         issued = i + 1;
       }
       if (*abort_flag) {
-        mbar_wait(&bars->fix_full, 0, tmo);
+        mbar_wait(&bars->fix_full, 0, tmo_unwind);
         for (int x = max(0, issued - 2); x < issued; ++x) {
-          mbar_wait(&bars->slot_full[slot_late(x)], (x >> 1) & 1, tmo);
-          mbar_wait(&bars->slot_full[slot_early(x)], (x >> 1) & 1, tmo);
+          mbar_wait(&bars->slot_full[slot_late(x)], (x >> 1) & 1, tmo_unwind);
+          mbar_wait(&bars->slot_full[slot_early(x)], (x >> 1) & 1, tmo_unwind);
         }
-        if (q_only >= 0) mbar_wait(&bars->slot_full[slot_late(q_only)], (q_only >> 1) & 1, tmo);
+        if (q_only >= 0) mbar_wait(&bars->slot_full[slot_late(q_only)], (q_only >> 1) & 1, tmo_unwind);
       }
     }
   } else if (warp == C::MMA_WARP) {
@@ -671,7 +673,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     }
     if (!ok && leader) fail(SITE_BW_MMA);
     if (leader) tc_commit(&bars->acc_done);
-    mbar_wait(&bars->acc_done, 0, tmo);
+    mbar_wait(&bars->acc_done, 0, tmo_unwind);
   } else {
     // ---- elementwise warps: one key row per thread pair (TMEM lane), column half
     //      hf; a step's 128 columns are the stacked query rows of one query tile

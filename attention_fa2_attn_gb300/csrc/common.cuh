@@ -116,6 +116,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// Waits that must complete before a CTA may exit or free its tensor memory --
+// bulk copies it issued landing in its shared memory, MMAs it issued draining --
+// depend on hardware progress only, not on another role of the CTA. Giving up on
+// them early would let a copy write shared memory the CTA no longer owns, or
+// free TMEM under a running MMA, so they are bounded by at least this much,
+// whatever shorter bound the caller chose for every other wait.
+constexpr uint64_t kUnwindWaitFloorNs = 1000000000ull;  // 1 s
+__host__ __device__ __forceinline__ uint64_t unwind_timeout(uint64_t timeout_ns) {
+  return timeout_ns > kUnwindWaitFloorNs ? timeout_ns : kUnwindWaitFloorNs;
+}
+
 // ----------------------------------------------------------------------------
 // TMA: tiled tensor loads and plain bulk copies (this CTA's own smem only)
 // ----------------------------------------------------------------------------

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(160, PAGED ? 2 : 1)
   const int ntiles = (k_end - k_begin + C::BC - 1) / C::BC;
   const int shift = S_b - p.T;
   const uint64_t tmo = p.timeout_ns;
+  const uint64_t tmo_unwind = unwind_timeout(tmo);  // copies landing before exit
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(160, PAGED ? 2 : 1)
         record_error(p.err, FA_ERR_TIMEOUT, SITE_DEC_PRODUCER);
         *abort_flag = 1;
         for (int it = max(0, issued - STAGES); it < issued; ++it)
-          mbar_wait(&full[it % STAGES], (it / STAGES) & 1, tmo);
+          mbar_wait(&full[it % STAGES], (it / STAGES) & 1, tmo_unwind);
       }
     }
   } else {

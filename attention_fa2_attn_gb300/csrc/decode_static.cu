@@ -39,7 +39,9 @@ static __device__ __align__(256) unsigned char g_fa_static_scratch[kFaStaticScra
 static std::mutex g_static_mu;
 
 // Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached. Null on failure.
+// per device (with that device current) and cached for the life of the
+// process. Null on failure. A device reset (cudaDeviceReset) after the first
+// call would leave the cached address dangling: it is not supported.
 static void* static_scratch_address(cudaError_t* why) {
   static void* addr[128] = {nullptr};
   int dev = 0;
@@ -79,13 +81,14 @@ fa_status fa_decode_splitkv_static(const void* q, const void* k, const void* v, 
   if (num_splits < 0 || num_splits > 1024) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if ((Hq / Hkv) * T > 16) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * Hkv > 65535 || static_cast<long long>(B) * Hkv * S >= (1ll << 31))
+  if (static_cast<long long>(B) * Hkv > 65535 || static_cast<long long>(B) * Hkv * S >= (1ll << 31) ||
+      static_cast<long long>(B) * Hq * T >= (1ll << 31))
     return FA_ERR_UNSUPPORTED;
   int n = num_splits;
   if (n == 0) {
     const int sms = device_sm_count();
     if (!sms) return static_cast<fa_status>(record_cuda_failure(cudaGetLastError()));
-    n = fa_num_splits_heuristic(B, Hkv, S, sms);
+    n = fa_decode_num_splits(B, Hq, Hkv, T, S, 0, sms);
   }
   // partials that do not fit the fixed array are refused, never truncated
   if (fa_decode_workspace_bytes(B, Hq, T, d, n) > kFaStaticScratchBytes) return FA_ERR_UNSUPPORTED;

@@ -75,6 +75,7 @@ struct KoBars {
   uint64_t pv_full[2];         // PV in TMEM
   uint64_t o_full[2];          // per O' buffer: the tile's O' landed (or nothing to load)
   uint64_t o_ready[2];         // per O' buffer: the update warps are done with it (128 arrivals)
+  uint64_t drain;              // every MMA the CTA issued has completed (before TMEM is freed)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
       mbar_init(&bars->o_full[x], 1);
       mbar_init(&bars->o_ready[x], 128);
     }
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -167,6 +169,7 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
   const uint64_t tmo = p.timeout_ns;
+  const uint64_t tmo_unwind = unwind_timeout(tmo);  // copies landing, MMAs draining
   auto fail = [&](unsigned site) {
     record_error(p.err, FA_ERR_TIMEOUT, site);
     *abort_flag = 1;
@@ -201,6 +204,9 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
       };
       KoIter s_it;
       int s = 0, jidx = -1, prev_j = -1;
+      // loads issued so far on kv_full, q_full and the o_full pair (steps armed):
+      // each barrier's earlier phases completed before its next load was issued
+      int kv_loads = 0, q_loads = 0, o_steps = 0;
       for (bool more = s_it.start(p, i_lo, i_hi); more && !*abort_flag; more = s_it.next(p), ++s) {
         const int i = s_it.i, j = s_it.j;
         const bool new_j = j != prev_j;
@@ -215,6 +221,7 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
             tma_load_3d(sK + c * C::CHUNK_BYTES, &tmK, &bars->kv_full, c * 64, j * 128, kv_plane);
             tma_load_3d(sV + c * C::CHUNK_BYTES, &tmV, &bars->kv_full, c * 64, j * 128, kv_plane);
           }
+          ++kv_loads;
         }
         if (s > 0 && !mbar_wait(&bars->q_empty, (s - 1) & 1, tmo, abort_flag)) {
           ok = false;
@@ -222,6 +229,7 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
         }
         mbar_arrive_expect_tx(&bars->q_full, C::Q_BYTES);
         for (int c = 0; c < C::KCH; ++c) tma_load_3d(sQ + c * C::CHUNK_BYTES, &tmQ, &bars->q_full, c * 64, i * 128, bh);
+        ++q_loads;
         // this step's O' buffer last held step s-2's tile
         if (s >= 2 && retired <= s - 2) {
           if (!retire(s - 2)) {
@@ -260,6 +268,7 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
           for (int c = 0; c < C::OCH; ++c)
             tma_load_3d(sO + (s & 1) * C::O_BYTES + c * C::CHUNK_BYTES, &tmO, of, c * 32, i * 128, bh);
         }
+        o_steps = s + 1;
         prev_j = j;
       }
       // hand back (and store) the last steps' buffers
@@ -267,6 +276,13 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
         if (!retire(t)) ok = false;
       bulk_wait_all();
       if (!ok) fail(SITE_KO_PRODUCER);
+      if (*abort_flag) {
+        // loads still in flight must land before the CTA exits: at most the last
+        // phase of kv_full and q_full, and the last step of each O' buffer
+        if (kv_loads > 0) mbar_wait(&bars->kv_full, (kv_loads - 1) & 1, tmo_unwind);
+        if (q_loads > 0) mbar_wait(&bars->q_full, (q_loads - 1) & 1, tmo_unwind);
+        for (int t = max(0, o_steps - 2); t < o_steps; ++t) mbar_wait(&bars->o_full[t & 1], (t >> 1) & 1, tmo_unwind);
+      }
     }
   } else if (warp == C::MMA_WARP) {
     // ======================= MMA issuer =======================
@@ -343,6 +359,10 @@ __global__ void __launch_bounds__(KoCfg<D>::THREADS, 1)
     }
     if (ok && !pv_prev_done && !*abort_flag && !issue_pv(s - 1)) ok = false;
     if (!ok) fail(SITE_KO_MMA);
+    // every MMA issued must finish before TMEM is released
+    if (leader) tc_commit(&bars->drain);
+    __syncwarp();
+    mbar_wait(&bars->drain, 0, tmo_unwind);
   } else {
     // ============ softmax and O' update: warps 0-3, thread r = row r ============
     const int r = threadIdx.x;  // 0..127

@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
   const uint64_t tmo = p.timeout_ns;
+  const uint64_t tmo_unwind = unwind_timeout(tmo);  // copies landing, MMAs draining
 
   const int shift_all = p.S - p.T;  // contiguous: bottom-right alignment, one shift for every item
 
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           if (g >= C::STAGES && !mbar_wait(&bars->v_empty[s], (u - 1) & 1, tmo, abort_flag)) {
             fail(SITE_PF_PRODUCER);
-            mbar_wait(&bars->k_full[s], u & 1, tmo);  // K was issued: let it land
+            mbar_wait(&bars->k_full[s], u & 1, tmo_unwind);  // K was issued: let it land
             break;
           }
           if (PAGED) {
@@ -353,10 +354,10 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (*abort_flag) {
         // copies still in flight must complete before the CTA exits
-        if (q_loads > 0) mbar_wait(&bars->q_full, (q_loads - 1) & 1, tmo);
+        if (q_loads > 0) mbar_wait(&bars->q_full, (q_loads - 1) & 1, tmo_unwind);
         for (uint32_t x = g > C::STAGES ? g - C::STAGES : 0; x < g; ++x) {
-          mbar_wait(&bars->k_full[x % C::STAGES], (x / C::STAGES) & 1, tmo);
-          mbar_wait(&bars->v_full[x % C::STAGES], (x / C::STAGES) & 1, tmo);
+          mbar_wait(&bars->k_full[x % C::STAGES], (x / C::STAGES) & 1, tmo_unwind);
+          mbar_wait(&bars->v_full[x % C::STAGES], (x / C::STAGES) & 1, tmo_unwind);
         }
       }
     }
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(384, 1)
     if (!ok && leader) fail(SITE_PF_MMA);
     // every MMA issued must finish before TMEM is released
     commit(&bars->drain);
-    mbar_wait(&bars->drain, 0, tmo);
+    mbar_wait(&bars->drain, 0, tmo_unwind);
   }
   } else {
     // ======================= softmax: warps 0-3 (tile 0), 4-7 (tile 1) =======================

@@ -181,6 +181,18 @@ FA_API int fa_num_splits_heuristic(int B, int Hkv, int S, int num_sms);
 FA_API int fa_num_splits_prefill(int B, int Hq, int Hkv, int T, int S, int num_sms);
 
 /*
+ * fa_decode_num_splits -- the key ranges fa_decode_splitkv (paged = 0) or
+ * fa_decode_paged (paged = 1, S = max_pages * page_size) take for
+ * num_splits == 0 when the workspace holds them: with (Hq / Hkv) * T <= 16,
+ * fa_num_splits_heuristic(B, Hkv, S, num_sms); with more rows,
+ * fa_num_splits_prefill(B, Hq, Hkv, T, S, num_sms) for contiguous K/V and 1
+ * for paged K/V. The one place this choice is made: a binding that sizes the
+ * workspace calls it and passes num_splits == 0 through. Pure host
+ * arithmetic. Returns 1 for invalid arguments.
+ */
+FA_API int fa_decode_num_splits(int B, int Hq, int Hkv, int T, int S, int paged, int num_sms);
+
+/*
  * fa_decode_workspace_bytes -- bytes of `workspace` a split decode needs:
  * FP32 partial outputs [num_splits][B*Hq*T][d] followed (256-byte aligned) by
  * FP32 partial lse [num_splits][B*Hq*T]. 0 when num_splits <= 1.
@@ -202,9 +214,11 @@ FA_API size_t fa_decode_workspace_bytes(int B, int Hq, int T, int d, int num_spl
  *   be one of 1, 2, 4, 8, 16 (else FA_ERR_UNSUPPORTED). num_splits > 1 cuts
  *   the keys into that many ranges of whole 128-key tiles for shapes whose
  *   query tiles do not fill the GPU, with the workspace and merge as above;
- *   num_splits == 0 takes fa_num_splits_prefill, lowered to what `workspace`
- *   holds (no workspace: no split). The result is the same attention.
- *   num_splits: 0 = fa_num_splits_heuristic(B, Hkv, S, SM count); else 1..1024.
+ *   num_splits == 0 takes fa_decode_num_splits (fa_num_splits_prefill here),
+ *   lowered to what `workspace` holds (no workspace: no split). The result is
+ *   the same attention.
+ *   num_splits: 0 = fa_decode_num_splits(B, Hq, Hkv, T, S, 0, SM count), here
+ *   fa_num_splits_heuristic(B, Hkv, S, SM count); else 1..1024.
  *   workspace: device scratch of at least fa_decode_workspace_bytes(...)
  *   bytes, 256-byte aligned (may be NULL when the split count is 1).
  *   Returns FA_ERR_INVALID_ARG if ws_bytes is too small.
@@ -223,14 +237,21 @@ FA_API fa_status fa_decode_splitkv(const void* q, const void* k, const void* v, 
  * (every device that loads the library holds one until the process exits);
  * the call allocates nothing.
  *   Arguments and results as fa_decode_splitkv, except that (Hq / Hkv) * T
- *   must be <= 16 (FA_ERR_UNSUPPORTED otherwise).
+ *   must be <= 16 (FA_ERR_UNSUPPORTED otherwise); B * Hq * T and
+ *   B * Hkv * S must be below 2^31 and B * Hkv at most 65535 (the same
+ *   limits, FA_ERR_UNSUPPORTED).
  *   Returns FA_ERR_UNSUPPORTED when the partials would need more than 4 MiB,
  *   i.e. fa_decode_workspace_bytes(B, Hq, T, d, splits) > 4194304.
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
+ *   The address is kept for the life of the process: resetting the device
+ *   (cudaDeviceReset) after that first call is not supported.
  *   All calls on a device share the array and it keeps the last call's
  *   contents (every call rewrites what it reads). Calls that overlap on the
  *   GPU -- other streams, other host threads -- race on it: serialise them.
+ *   If a kernel of the call records FA_ERR_TIMEOUT or FA_ERR_BOUNDS (see
+ *   fa_get_last_device_error), o and lse are undefined: the merge may have
+ *   read partials an earlier call left in the array.
  */
 FA_API fa_status fa_decode_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
                                           int B, int Hq, int Hkv, int T, int S, int d, float scale, int causal,
@@ -288,9 +309,20 @@ FA_API fa_status fa_get_last_device_error(void* stream, int* detail);
 
 /*
  * fa_set_wait_timeout_ns -- bound, in nanoseconds of %globaltimer, for every
- * wait inside the kernels launched after this call (default 4e9 = 4 s).
+ * wait of one role of a CTA on another inside the kernels launched after this
+ * call (default 4e9 = 4 s). Values below 1e6 (1 ms) are raised to 1e6. The
+ * waits a CTA makes before it exits or frees its tensor memory (its own bulk
+ * copies landing, its own MMAs draining) are bounded by max(this, 1e9): a
+ * short setting never lets a CTA leave with copies or MMAs still running.
  */
 FA_API void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * fa_get_wait_timeouts -- the bounds in force, in nanoseconds: *wait_ns the
+ * bound of fa_set_wait_timeout_ns as clamped, *unwind_ns the bound of the
+ * waits before a CTA exits (max(*wait_ns, 1e9)). Either pointer may be NULL.
+ */
+FA_API void fa_get_wait_timeouts(unsigned long long* wait_ns, unsigned long long* unwind_ns);
 
 /*
  * fa_selftest_wait_timeout -- failure-detection self test (no counterpart on

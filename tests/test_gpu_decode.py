@@ -179,3 +179,30 @@ def test_paged_bad_table_entry_is_reported():
     o_ref, l_ref = oracle.decode_paged(q, kp, vp, table, sl, 16, 1 / math.sqrt(d), True)
     compare(o, l, o_ref, l_ref, what="after bounds error")
     assert fa.fa_get_last_device_error()[0] == 0
+
+
+def test_zero_splits_same_choice_through_python_and_c():
+    """num_splits = 0 is resolved by the library alone: the Python call (which only
+    sizes the workspace from fa_decode_num_splits), a direct C call with an ample
+    workspace, and an explicit call with that count give the same bits."""
+    import ctypes
+
+    fa = _fa()
+    from attention_fa2_attn_gb300 import _lib
+
+    L = _lib.lib()
+    for B, Hq, Hkv, T, S, d in ((1, 32, 8, 1, 16384, 128), (1, 2, 2, 600, 3000, 64)):
+        q, k, v = (t.to(DEV) for t in fi.qkv(B, Hq, Hkv, T, S, d, 130 + d))
+        n = fa.fa_decode_num_splits(B, Hq, Hkv, T, S)
+        assert n > 1
+        o_py, l_py = fa.fa_decode_splitkv(q, k, v, causal=True, num_splits=0)
+        o_n, l_n = fa.fa_decode_splitkv(q, k, v, causal=True, num_splits=n)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(B, Hq, T, d, 64), dtype=torch.uint8, device=DEV)
+        o_c, l_c = torch.empty_like(q), torch.empty((B, Hq, T), dtype=torch.float32, device=DEV)
+        st = L.fa_decode_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_c.data_ptr(), l_c.data_ptr(), B, Hq,
+                                 Hkv, T, S, d, 1.0 / math.sqrt(d), 1, 0, ws.data_ptr(), ws.numel(),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0
+        torch.cuda.synchronize()
+        assert torch.equal(o_py, o_n) and torch.equal(l_py, l_n)
+        assert torch.equal(o_c, o_n) and torch.equal(l_c, l_n)

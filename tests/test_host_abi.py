@@ -163,3 +163,50 @@ def test_workspace_size_counts_bytes_of_any_dtype():
         _ws_bytes(torch.empty(9, dtype=torch.float32), 40, "cpu")
     with pytest.raises(ValueError):
         _ws_bytes(torch.empty(20, dtype=torch.float32)[::2], 40, "cpu")
+
+
+def test_wait_timeout_clamp_and_unwind_floor(L):
+    """The settable wait bound has a 1 ms floor; the waits a CTA makes before it
+    exits (its copies landing, its MMAs draining) are bounded by at least 1 s,
+    whatever is set."""
+    w, u = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    L.fa_get_wait_timeouts(ctypes.byref(w), ctypes.byref(u))
+    default = w.value
+    assert (default, u.value) == (4_000_000_000, 4_000_000_000)
+    try:
+        for set_ns, want_wait, want_unwind in (
+            (0, 10**6, 10**9),
+            (1, 10**6, 10**9),
+            (999_999, 10**6, 10**9),
+            (10**6, 10**6, 10**9),
+            (5 * 10**8, 5 * 10**8, 10**9),
+            (10**9, 10**9, 10**9),
+            (7 * 10**9, 7 * 10**9, 7 * 10**9),
+        ):
+            L.fa_set_wait_timeout_ns(set_ns)
+            L.fa_get_wait_timeouts(ctypes.byref(w), ctypes.byref(u))
+            assert (w.value, u.value) == (want_wait, want_unwind), set_ns
+        L.fa_get_wait_timeouts(None, None)  # either pointer may be NULL
+    finally:
+        L.fa_set_wait_timeout_ns(default)
+
+
+def test_decode_split_choice_is_made_in_one_place(L):
+    """fa_decode_num_splits is the choice num_splits = 0 makes: the decode rule for
+    at most 16 stacked rows per KV head, the prefill rule above that (contiguous
+    K/V), no split for paged K/V with many rows."""
+    ds = L.fa_decode_num_splits
+    assert ds(1, 32, 8, 1, 131072, 0, 152) == L.fa_num_splits_heuristic(1, 8, 131072, 152) == 19
+    assert ds(64, 64, 8, 1, 8192, 1, 152) == L.fa_num_splits_heuristic(64, 8, 8192, 152) == 1
+    assert ds(1, 8, 2, 4, 5000, 1, 152) == L.fa_num_splits_heuristic(1, 2, 5000, 152)  # 16 rows: decode kernel
+    assert ds(1, 8, 2, 5, 5000, 0, 152) == L.fa_num_splits_prefill(1, 8, 2, 5, 5000, 152)  # 20 rows: prefill kernel
+    assert ds(1, 1, 1, 8192, 8192, 0, 152) == L.fa_num_splits_prefill(1, 1, 1, 8192, 8192, 152) == 4
+    assert ds(1, 1, 1, 8192, 8192, 1, 152) == 1
+    assert ds(0, 1, 1, 1, 100, 0, 152) == 1
+    assert ds(1, 6, 4, 1, 100, 0, 152) == 1  # Hq not a multiple of Hkv
+    # the binding sizes its workspace from the library's answer; it holds no rule of its own
+    from attention_fa2_attn_gb300 import api
+
+    for args in ((1, 32, 8, 1, 131072, False), (1, 1, 1, 8192, 8192, False), (3, 16, 4, 2, 9000, True),
+                 (1, 16, 2, 40, 2304, True), (2, 4, 4, 300, 2200, False)):
+        assert api.fa_decode_num_splits(*args, num_sms=152) == ds(*args[:5], int(args[5]), 152), args

@@ -231,6 +231,13 @@ def run_oracle_child(mode: str, a: float, b: float = 0.0) -> dict:
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def bench_config(w, world: int) -> dict:
+    """The workload description both arms print: the same keys and values."""
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "S": w.S, "d": w.d,
+            "causal": w.causal, "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2 (Q, K, V, O: 268 MB per step)"}
+
+
 def reference_arm(args, rank: int, world: int) -> int:
     if rank != 0:
         return 0
@@ -259,8 +266,7 @@ def reference_arm(args, rank: int, world: int) -> int:
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "S": w.S, "d": w.d,
-                   "causal": w.causal, "sample": f"{rows[0]} rows per step"},
+        "config": bench_config(w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -666,9 +672,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "S": w.S, "d": w.d,
-                       "causal": w.causal, "parallelism": f"replicas{world}",
-                       "l2": "inputs larger than L2 (Q, K, V, O: 268 MB per step)"},
+            "config": bench_config(w, world),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
                          "traffic": traffic, "kernel": "prefill_tc_kernel<128>",

@@ -106,6 +106,10 @@ struct BwCfg {
   static constexpr int COL_S = 0;                // S (or S^T): fp32; P / dS (bf16) later over it
   static constexpr int COL_DP = 128;             // dP (or dP^T)
   static constexpr int COL_ACC = 256;            // dQ, or dV then dK
+  // dQ: Q and dO (fixed for the whole tile) packed bf16 in TMEM, the A operands of S
+  // and dP, so that those products read only their B operand from shared memory
+  static constexpr int COL_QA = 384;
+  static constexpr int COL_DOA = 448;
   // Packed bf16 operands (two per 32-bit column) written by column half hf over
   // the first 32 of its own 64 fp32 columns: the 16 keys (or queries) of MMA
   // K-step kk sit at column packed_col(kk) of the S (or dP) region.
@@ -143,6 +147,7 @@ struct BwBars {
   uint64_t s_read;        // dK/dV: S^T read out of TMEM (S^T of the next step may overwrite it)
   uint64_t pt_free;       // dK/dV: dV has read P^T from shared memory
   uint64_t e_second;      // dS (or dS^T) written
+  uint64_t a_ready;       // dQ: Q and dO copied into TMEM (the A operands of S and dP)
   uint64_t acc_done;      // the last accumulation finished
   uint64_t slot_full[4];  // a streamed tile landed in ring slot t
   uint64_t slot_empty[4]; // the last MMA reading slot t finished
@@ -195,6 +200,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->e_first, C::EW_THREADS);
     mbar_init(&bars->e_second, C::EW_THREADS);
+    mbar_init(&bars->a_ready, C::EW_THREADS);
     mbar_init(&bars->acc_done, 1);
     for (int t = 0; t < 4; ++t) {
       mbar_init(&bars->slot_full[t], 1);
@@ -260,24 +266,24 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     }
   } else if (warp == C::MMA_WARP) {
     const bool leader = elect_one();
-    constexpr uint32_t idesc_ss = idesc_bf16_f32(128, C::BN, 0, 0);  // A, B K-major
-    constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, 0, 1);      // A from TMEM, B MN-major
-    const uint64_t dQd = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-    const uint64_t dDOd = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+    constexpr uint32_t idesc_ss = idesc_bf16_f32(128, C::BN, 0, 0);  // S, dP: A from TMEM, B K-major
+    constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, 0, 1);      // dQ: A from TMEM, B MN-major
     const uint64_t dRing = smem_desc_sw128(smem_u32(sRing), 16, 1024);                    // K (for S), V (for dP)
     const uint64_t dRingKmn = smem_desc_sw128(smem_u32(sRing), C::CHUNK_BYTES, 1024);     // K as the B of dQ
     auto slot_off = [](int t) { return static_cast<uint64_t>((t * C::TILE_BYTES) >> 4); };
     // Issue order: S(0), dP(0), then per key tile j: S(j+1) (once the warps have read
     // S(j) out), dQ(j) += dS(j) K_j (dS over dP's columns), dP(j+1) (after dQ(j) in
     // issue order, so it never overwrites dS(j) before it is read). The MMAs of the
-    // neighbouring tiles run while the warps work on tile j.
+    // neighbouring tiles run while the warps work on tile j. S and dP take Q and dO
+    // from TMEM (16 d-values = 8 packed columns per K step): every product reads only
+    // its B operand (K or V) from shared memory.
     auto issue_s = [&](int j) {
       const uint64_t so = slot_off(slot_late(j));
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_S, dQd + off, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+          tc_mma_ts(tmem + C::COL_S, tmem + C::COL_QA + kk * 8, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
         tc_commit(&bars->s_full);
       }
@@ -290,13 +296,14 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          tc_mma_ss(tmem + C::COL_DP, dDOd + off, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
+          tc_mma_ts(tmem + C::COL_DP, tmem + C::COL_DOA + kk * 8, dRing + so + off, idesc_ss, kk > 0 ? 1u : 0u);
         }
         tc_commit(&bars->dp_full);
         tc_commit(&bars->slot_empty[vs]);
       }
     };
-    bool ok = mbar_wait(&bars->fix_full, 0, tmo, abort_flag);
+    // Q and dO reach TMEM through the elementwise warps (after fix_full)
+    bool ok = mbar_wait(&bars->a_ready, 0, tmo, abort_flag);
     if (ok && nj > 0) {
       ok = mbar_wait(&bars->slot_full[slot_late(0)], 0, tmo, abort_flag) &&
            mbar_wait(&bars->slot_full[slot_early(0)], 0, tmo, abort_flag);
@@ -363,8 +370,37 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     const float2 c2 = make_float2(p.c, p.c);
     const float2 nl2 = make_float2(nl2_row, nl2_row);
     const float2 nd2 = make_float2(nd_row, nd_row);
-    bool ok = true;
-    for (int j = 0; j < nj; ++j) {
+    // Q and dO rows into TMEM as packed bf16 pairs (column c holds d-values 2c, 2c+1):
+    // row r of the 128-byte-swizzled smem tiles, this column half's D/4 columns
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->fix_full, 0, tmo, abort_flag));
+    if (ok) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint8_t* src = which ? sDO : sQ;
+        uint32_t wv[D / 4];
+        // d = 128: half hf is chunk hf (64 values); d = 64: half hf is units 4hf..4hf+3 of the one chunk
+#pragma unroll
+        for (int u = 0; u < D / 16; ++u) {
+          const int unit = D == 128 ? u : 4 * hf + u;
+          const uint8_t* rowp = src + (D == 128 ? hf * C::CHUNK_BYTES : 0) + r * 128;
+          const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((unit ^ (r & 7)) << 4));
+          wv[4 * u + 0] = x.x;
+          wv[4 * u + 1] = x.y;
+          wv[4 * u + 2] = x.z;
+          wv[4 * u + 3] = x.w;
+        }
+        const uint32_t col = (which ? C::COL_DOA : C::COL_QA) + hf * (D / 4);
+        if constexpr (D == 128) {
+          tmem_st32(tmem + lane_base + col, wv);
+        } else {
+          tmem_st16(tmem + lane_base + col, wv);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->a_ready);
+    }
+    for (int j = 0; ok && j < nj; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, tmo, abort_flag))) {
         ok = false;
         break;

@@ -11,7 +11,8 @@
 //
 // How (GB300-specific): two launches.
 //   * bwd_rowsum_kernel: per query row, -D and the negated base-2 LSE into a small
-//     workspace (HBM-bound, tiny).
+//     workspace (HBM-bound, tiny); the main grid launches as its programmatic
+//     dependent.
 //   * bwd_kernel: the dK/dV pass and the dQ pass as the two halves of one grid,
 //     the dQ CTAs filling the last wave of the dK/dV ones.
 //     - dK/dV (bwd_dkdv_cta): one 128-key tile per CTA looping over the query tiles
@@ -40,12 +41,15 @@ namespace fa {
 // (plane 0) and -lse * log2(e), the row's LSE in base 2 negated (plane 1; -inf for
 // a row with no visible key, so that its P is 0). A group of d / 8 lanes takes a
 // row, one 16-byte load of O and of dO per lane (HBM-bound: every byte of O and dO
-// is read once).
+// is read once). Every block lets the main kernel launch as its programmatic
+// dependent at once; that kernel waits (griddepcontrol.wait) only where it reads
+// these values.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) bwd_rowsum_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ d_o,
                                                          const float* __restrict__ lse, float* __restrict__ vecs,
                                                          long long rows, int T, int T_pad, int d) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lanes = d / 8;  // 16 (d = 128) or 8 (d = 64): a power of two dividing 32
   const int sub = threadIdx.x & (lanes - 1);
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / lanes;
@@ -362,6 +366,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     const size_t row_index = (static_cast<size_t>(b) * p.Hq + h) * p.T + (row_valid ? pos : 0);
     // P = 2^(S*c - lse*log2e); rows past T and rows with no visible key get P = 0
     const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.T_pad + (row_valid ? pos : 0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row pass's values are complete and visible
     const float nl2_row = row_valid ? __ldg(p.nl2 + vi) : -INFINITY;
     const float nd_row = row_valid ? __ldg(p.neg_d + vi) : 0.f;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -586,6 +591,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
           fail(SITE_BW_PRODUCER);
           break;
         }
+        if (i == 0) asm volatile("griddepcontrol.wait;" ::: "memory");  // the row pass's values are visible
         // dO, and the tile's -lse2 (plane B + b) and -D (plane b) in stacked row order
         // (positions past T read as 0; their Q and dO rows are zero as well). The
         // vectors' buffer i & 1 was last read by the warps in step i - 2, before dK(i - 2)
@@ -931,7 +937,20 @@ static int launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tdo, const CUt
   const unsigned nbkv = static_cast<unsigned>(p.B * p.Hkv);
   const long long ctas = static_cast<long long>(p.n_ktiles + p.n_qtiles) * nbkv;
   if (ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  kfn<<<static_cast<unsigned>(ctas), C::THREADS, C::SMEM, stream>>>(tq, tdo, tk, tv, tvec, p);
+  // a programmatic dependent of the row pass: its CTAs start (barriers, TMEM, the fixed
+  // tiles, the first products) while the row pass finishes, and wait only where they
+  // read its values
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kfn, tq, tdo, tk, tv, tvec, p) != cudaSuccess) return FA_ERR_CUDA;
   return launch_status();
 }
 

@@ -362,6 +362,27 @@ def secondary_measurements(torch, fa, dev, stream, steps: int, peaks) -> dict:
                    "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "frac_of_nominal_bf16": tf / NOMINAL_BF16_TFLOPS, "launches_per_step": 1}
     del q, k, v, o, lse
 
+    # the prefill workload's shapes at head dimension 64 (half the tensor work per key,
+    # the same softmax work): B = 4, H = 16, N = 4096, non-causal
+    w = fi.PREFILL_MHA
+    d64 = 64
+    q = rnd((w.B, w.Hq, w.T, d64), 1000 + w.index)
+    k = rnd((w.B, w.Hkv, w.S, d64), 2000 + w.index)
+    v = rnd((w.B, w.Hkv, w.S, d64), 3000 + w.index)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.T, device=dev)
+    step = lambda: fa.fa_fwd(q, k, v, causal=False, scale=d64 ** -0.5, out=o, lse=lse)  # noqa: E731
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(torch, step, steps, stream)
+    tf = cm.attention_flops(w.B, w.Hq, w.T, w.S, d64, False) / (ms * 1e-3) / 1e12
+    out["prefill_mha_b4_h16_n4096_d64"] = {
+        "metric": "attn fwd TFLOP/s", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+        "frac_of_measured_bf16": tf / peaks["bf16_tflops"], "frac_of_nominal_bf16": tf / NOMINAL_BF16_TFLOPS,
+        "launches_per_step": 1}
+    del q, k, v, o, lse
+
     # split-KV decode (decode kernel + merge)
     w = fi.SPLITKV_DECODE
     q = rnd((w.B, w.Hq, w.T, w.d), 1000 + w.index)

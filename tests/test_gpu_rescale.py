@@ -125,3 +125,46 @@ def test_climbing_max_paged(d):
     o, l = _fa().fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), seqlens.to(DEV), causal=True,
                                  scale=scale)
     compare(o, l, o_ref, l_ref, what=f"paged d{d}")
+
+
+@pytest.mark.parametrize("d,n", [(64, 1), (128, 1), (128, 5)])
+def test_climbing_max_decode(d, n):
+    """The decode kernel rescales its register-held O on every rise of the maximum:
+    hot keys every 64-key decode tile, levels climbing by steps below and above 8
+    (log2 units), one new token per sequence, GQA group 4, ragged key count, unsplit
+    and split into ranges with the LSE merge."""
+    B, Hq, Hkv, T, S = 2, 8, 2, 1, 4096 + 37
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = fi.climbing_qkv(B, Hq, Hkv, T, S, d, 250 + d + n, scale, pattern="rise", hot=2, v_scale=0.5,
+                              tile=64)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, True)
+    o, l = _fa().fa_decode_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, num_splits=n, scale=scale)
+    compare(o, l, o_ref, l_ref, what=f"decode d{d} n{n}")
+
+
+def test_climbing_max_paged_decode():
+    """The same through the paged decode kernel (16-token pages, one table for K and V),
+    sequences of different lengths."""
+    B, Hq, Hkv, T, S, d = 3, 16, 4, 1, 3000, 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = fi.climbing_qkv(B, Hq, Hkv, T, S, d, 260, scale, pattern="rise_fall", hot=1, v_scale=0.5, tile=64)
+    kp, vp, table = fi.pages_from_contiguous(k, v, 16, 260)
+    seqlens = torch.tensor([S, 2049, 700], dtype=torch.int32)
+    o_ref, l_ref = oracle.decode_paged(q, kp, vp, table, seqlens, 16, scale, True)
+    o, l = _fa().fa_decode_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), seqlens.to(DEV), causal=True,
+                                 num_splits=3, scale=scale)
+    compare(o, l, o_ref, l_ref, what="paged decode")
+
+
+@pytest.mark.parametrize("bands", [1, 2])
+def test_climbing_max_kv_outer(bands):
+    """The FlashAttention-1 loop order keeps the normalised running O', m, l of every row
+    in HBM and rescales O' by l * 2^(m - m_new) / l_new at each key tile: with the
+    maximum climbing on every tile that factor is far from 1 on every step."""
+    B, Hq, Hkv, T, S, d = 1, 2, 2, 256, 2304, 128
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = fi.climbing_qkv(B, Hq, Hkv, T, S, d, 270, scale, pattern="rise", hot=2, mixed_rows=True,
+                              v_scale=0.5)
+    o_ref, l_ref = oracle.attention_three_pass(q, k, v, scale, True)
+    o, l = _fa().fa_fwd_kv_outer(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=scale, row_bands=bands)
+    compare(o, l, o_ref, l_ref, what=f"kv_outer bands {bands}")

@@ -135,6 +135,14 @@ def test_causal_gqa_full_size_sampled():
     _sampled_check(fi.CAUSAL_GQA, 2048, 6)
 
 
+def test_prefill_mha_d64_full_size_sampled():
+    """The prefill workload's shapes at head dimension 64 (B=4, H=16, N=4096,
+    non-causal), the d = 64 instantiation in the launch configuration it is timed in."""
+    w = fi.PREFILL_MHA
+    _sampled_check(fi.Workload(w.name.replace("d128", "d64"), w.index, w.B, w.Hq, w.Hkv, w.T, w.S, 64, False),
+                   2048, 8)
+
+
 @pytest.mark.parametrize("N,d", fi.PREFILL_MHA.sweep)
 def test_one_head_sweep_sampled(N, d):
     w = fi.Workload(f"sweep_{N}_{d}", 10 + d // 64, 1, 1, 1, N, N, d, False)

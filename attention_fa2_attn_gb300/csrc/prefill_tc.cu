@@ -128,6 +128,22 @@ __device__ __forceinline__ int split_j0(const PfParams& p, int it) {
   return SPLIT ? (it % p.num_splits) * p.split_tiles : 0;
 }
 
+// Snake dealing of items sorted heaviest first: slot `it` of CTA x in round
+// it / G takes sorted item round * G + x, or round * G + (G - 1 - x) when the
+// round runs backwards. The snake is anchored at the end: the last full round
+// runs backwards, the one before it forwards, and so on. So the CTAs with the
+// lowest indexes end the full rounds the least loaded, and they are the ones
+// that take the last, partial round (forwards, as only CTAs 0 .. n % G - 1 get
+// a slot in it). A reversed round stays inside its own G items, so the map is
+// one to one.
+__device__ __forceinline__ int snake_sorted(int it, int n_items) {
+  const int G = gridDim.x;
+  const int round = it / G;
+  const int x = it - round * G;
+  const int full_rounds = n_items / G;
+  return ((full_rounds - round) & 1) ? round * G + (G - 1 - x) : it;
+}
+
 template <bool PAGED, bool SPLIT = false>
 __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn, const int* order) {
   PfItem w;
@@ -142,11 +158,8 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn, con
     // Sequences of a paged batch differ in length, so item weights differ by
     // sequence: items go longest sequence first (order[] ranks them when the batch
     // has at most MAX_RANKED sequences), within it heaviest query-tile pair first,
-    // dealt to the CTAs in the same snake order as below.
-    const int G = gridDim.x;
-    const int round = it / G;
-    const int x = it - round * G;
-    const int sorted = ((round & 1) && (round + 1) * G <= p.n_items) ? round * G + (G - 1 - x) : it;
+    // dealt to the CTAs in snake order.
+    const int sorted = snake_sorted(it, p.n_items);
     const int per_b = p.Hkv * p.n_pairs;
     const int rank = sorted / per_b;
     const int within = sorted - rank * per_b;
@@ -155,12 +168,8 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int it, int bn, con
     w.bh = b * p.Hkv + within % p.Hkv;
   } else if (p.causal) {
     // items sorted heaviest first, dealt to the CTAs in snake order (rounds of
-    // gridDim.x alternate direction) so that every CTA's total is close to the mean;
-    // the last, partial round keeps the forward direction
-    const int G = gridDim.x;
-    const int round = it / G;
-    const int x = it - round * G;
-    const int sorted = ((round & 1) && (round + 1) * G <= p.n_items) ? round * G + (G - 1 - x) : it;
+    // gridDim.x alternate direction) so that every CTA's total is close to the mean
+    const int sorted = snake_sorted(it, p.n_items);
     qp = p.n_pairs - 1 - sorted / bh_count;
     w.bh = sorted % bh_count;
   } else {  // head-major: CTAs working at the same time share a head's K/V in L2

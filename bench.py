@@ -690,11 +690,10 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
     traffic = load_traffic().get("prefill_tc_kernel")
 
     # end to end: pinned host inputs -> HBM -> kernel -> O and lse back to pinned host memory.
-    # Each step's batch is pipelined over three streams in chunks: a chunk's inputs are copied
-    # in on s_in, its fa_fwd runs on the bench stream once they have landed, and its O and lse
-    # are copied out on s_out. So the copies of one chunk overlap the kernel of another. A chunk
-    # is a whole batch element, except that the last element goes in two halves of its KV
-    # heads (with their query heads).
+    # Each step's batch is pipelined over three streams in chunks of one batch element: a
+    # chunk's inputs are copied in on s_in, its fa_fwd runs on the bench stream once they have
+    # landed, and its O and lse are copied out on s_out. So the copies of one chunk overlap the
+    # kernel of another.
     # Consecutive steps alternate between two sets of device buffers, so step i+1's inputs
     # stream in while step i's last kernels and copies out still run. A set is written again
     # only after the kernels of the step before last have read its inputs and that step's
@@ -706,9 +705,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> int:
     bufs = [(q, k, v, o, lse), tuple(torch.empty_like(x) for x in (q, k, v, o, lse))]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     grp = w.Hq // w.Hkv
-    chunks = [(b, 0, w.Hkv) for b in range(w.B - 1)]  # (batch element, KV heads [kv0, kv1))
-    half = w.Hkv // 2
-    chunks += [(w.B - 1, 0, half), (w.B - 1, half, w.Hkv)] if half >= 1 else [(w.B - 1, 0, w.Hkv)]
+    chunks = [(b, 0, w.Hkv) for b in range(w.B)]  # (batch element, KV heads [kv0, kv1))
     ev_in = [[torch.cuda.Event() for _ in chunks] for _ in bufs]
     ev_k = [[torch.cuda.Event() for _ in chunks] for _ in bufs]
     inputs_read = [torch.cuda.Event() for _ in bufs]  # the set's last kernel of its latest step

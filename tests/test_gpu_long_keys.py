@@ -1,8 +1,8 @@
 """Parity at key counts far past the workloads': 2^20 + 37 keys per sequence, so
 each K and V tensor (and each paged pool) is over 2 GiB and byte offsets into it
 pass 2^31. This exercises the 64-bit address arithmetic of every path, the ring
-counters and barrier phases over 8193 key tiles per item, and split ranges of
-over 65536 keys.
+counters and barrier phases over 8193 key tiles per item, split ranges of over
+65536 keys, and the backward's 98316 dK/dV CTAs and 8193-step dQ loops.
 
 Inputs are drawn on the device from the seeded generators. The oracle checks a
 sample of query rows: each row is independent, so it is exact against the whole
@@ -18,6 +18,7 @@ import torch
 import fa_inputs as fi
 import oracle
 from parity import compare
+from test_gpu_backward import _grad_compare  # the backward's bounds, relative to each gradient's largest entry
 
 pytestmark = pytest.mark.gpu
 
@@ -111,3 +112,30 @@ def test_paged_long_pool():
         _check_rows(o_r[b : b + 1], l_r[b : b + 1], q[b : b + 1], k[b : b + 1, :, :sb], v[b : b + 1, :, :sb], rows,
                     scale, True, f"paged ragged b{b}")
     del q, k, v, kp, vp
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_long_keys(causal):
+    """fa_fwd then fa_bwd with 256 query rows per head over 2^20 + 37 keys, 12
+    heads: K, V, dK and dV are 3.2 GB each, and head 10 lies wholly past 2^31
+    bytes. dQ rows (each over every key) and dK/dV rows (each over every query row)
+    of heads 1 and 10 are checked against the oracle, given those heads' planes."""
+    B, H, T, S, d = 1, 12, 256, S_LONG, 128
+    q, k, v = fi.qkv(B, H, H, T, S, d, 930 + int(causal), device=DEV)
+    do = fi.randn((B, H, T, d), 5930 + int(causal), device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    fa = _fa()
+    o, lse = fa.fa_fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, causal=causal, scale=scale)
+    for h in (1, 10):
+        sl = slice(h, h + 1)
+        q_rows = [(0, 0, i) for i in (0, 77, 128, 255)]
+        k_rows = [(0, 0, j) for j in (0, 12345, S - T - 1, S - T, S - 100, S - 1)]
+        rq, rk, rv = oracle.attention_backward_rows(q[:, sl], k[:, sl], v[:, sl], do[:, sl], o[:, sl].float(),
+                                                    lse[:, sl], q_rows, k_rows, scale, causal)
+        iq = torch.tensor([i for _, _, i in q_rows])
+        ik = torch.tensor([j for _, _, j in k_rows])
+        _grad_compare(dq[0, h].cpu()[iq], rq, f"dq head {h} causal={causal}")
+        _grad_compare(dk[0, h].cpu()[ik], rk, f"dk head {h} causal={causal}")
+        _grad_compare(dv[0, h].cpu()[ik], rv, f"dv head {h} causal={causal}")
+    del q, k, v, do, o, dq, dk, dv

@@ -13,7 +13,6 @@ bound on O; at a quarter of the size O stays below about 1.2, where that roundin
 is at most 0.0039 and the bound measures the computation.
 """
 
-
 import pytest
 import torch
 

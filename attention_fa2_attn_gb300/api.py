@@ -40,16 +40,41 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
 
 
+def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    """q [B][Hq][T][d], k and v [B][Hkv][S][d] on one device. The library takes every
+    size from q and k, so v must match k exactly and q must share B and d."""
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must be on one device")
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError(f"k and v must have one shape, got {tuple(k.shape)} and {tuple(v.shape)}")
+    if q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError(f"q {tuple(q.shape)} and k {tuple(k.shape)} must share batch and head dimension")
+
+
+def _out(t, name: str, shape, dtype, like: torch.Tensor) -> torch.Tensor:
+    """A caller's output tensor, checked (the library writes it through a bare pointer,
+    so a smaller or strided tensor would be written past its end), or a new one."""
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    if not isinstance(t, torch.Tensor) or t.device != like.device:
+        raise ValueError(f"{name} must be a tensor on {like.device}")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+    return t
+
+
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, want_lse: bool = True):
     """Prefill forward: q [B][Hq][T][d], k, v [B][Hkv][S][d] bf16 -> (o bf16, lse fp32 or None)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
+    _check_qkv(q, k, v)
     B, Hq, T, d = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    if want_lse and lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    o = _out(out, "out", q.shape, torch.bfloat16, q)
+    if want_lse or lse is not None:
+        lse = _out(lse, "lse", (B, Hq, T), torch.float32, q)
     st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale, int(causal), _stream(q))
     check(st, "fa_fwd")
     return o, lse
@@ -59,6 +84,7 @@ def fa_fwd_f32(q, k, v, causal: bool = False, scale: float | None = None):
     """The same forward in fp32 on the CUDA cores: fp32 q, k, v -> (o fp32, lse fp32)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.float32, 4)
+    _check_qkv(q, k, v)
     B, Hq, T, d = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -90,16 +116,22 @@ def fa_bwd(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = Non
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (d_o, "d_o")):
         _need(t, n, torch.bfloat16, 4)
     _need(lse, "lse", torch.float32, 3)
+    _check_qkv(q, k, v)
     B, Hq, T, d = q.shape
+    for t, n in ((o, "o"), (d_o, "d_o")):
+        if t.device != q.device or tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{n} must have q's shape {tuple(q.shape)} on its device")
+    if lse.device != q.device or tuple(lse.shape) != (B, Hq, T):
+        raise ValueError(f"lse must be [B][Hq][T] = {(B, Hq, T)} on q's device")
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     nbytes = fa_bwd_workspace_bytes(B, Hq, T)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = _ws_bytes(workspace, nbytes, q.device)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = _out(dq, "dq", q.shape, torch.bfloat16, q)
+    dk = _out(dk, "dk", k.shape, torch.bfloat16, q)
+    dv = _out(dv, "dv", v.shape, torch.bfloat16, q)
     st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
                       Hkv, T, S, d, scale, int(causal), _ptr(workspace), ws_bytes, _stream(q))
     check(st, "fa_bwd")
@@ -116,6 +148,7 @@ def fa_fwd_kv_outer(q, k, v, causal: bool = False, scale: float | None = None, r
     state through HBM): q [B][Hq][T][d], k, v [B][Hkv][S][d] bf16 -> (o, lse)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
+    _check_qkv(q, k, v)
     B, Hq, T, d = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -123,8 +156,8 @@ def fa_fwd_kv_outer(q, k, v, causal: bool = False, scale: float | None = None, r
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = _ws_bytes(workspace, nbytes, q.device)
-    o = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    o = _out(out, "out", q.shape, torch.bfloat16, q)
+    lse = _out(lse, "lse", (B, Hq, T), torch.float32, q)
     st = lib().fa_fwd_kv_outer(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
                                int(causal), int(row_bands), _ptr(workspace), ws_bytes, _stream(q))
     check(st, "fa_fwd_kv_outer")
@@ -166,15 +199,15 @@ def fa_decode_splitkv(q, k, v, causal: bool = True, num_splits: int = 0, scale: 
     """Split-KV decode: q [B][Hq][T][d], k, v [B][Hkv][S][d] bf16 -> (o, lse)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
+    _check_qkv(q, k, v)
     B, Hq, T, d = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     # the workspace is sized for the count the library takes; num_splits passes through as given
     n = int(num_splits) or fa_decode_num_splits(B, Hq, Hkv, T, S, False, device=q.device)
     ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
-    o = torch.empty_like(q) if out is None else out
-    if lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    o = _out(out, "out", q.shape, torch.bfloat16, q)
+    lse = _out(lse, "lse", (B, Hq, T), torch.float32, q)
     st = lib().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
                                  int(causal), int(num_splits), _ptr(ws), ws_bytes, _stream(q))
     check(st, "fa_decode_splitkv")
@@ -187,12 +220,12 @@ def fa_decode_splitkv_static(q, k, v, causal: bool = True, num_splits: int = 0, 
     (no workspace, no allocation inside the call); see include/fa_gb300.h."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
+    _check_qkv(q, k, v)
     B, Hq, T, d = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    if lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    o = _out(out, "out", q.shape, torch.bfloat16, q)
+    lse = _out(lse, "lse", (B, Hq, T), torch.float32, q)
     st = lib().fa_decode_splitkv_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, T, S, d, scale,
                                         int(causal), int(num_splits), _stream(q))
     check(st, "fa_decode_splitkv_static")
@@ -224,12 +257,17 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = Tr
     B, Hq, T, d = q.shape
     P, page_size, Hkv, _ = k_pages.shape
     max_pages = block_table.shape[1]
+    if not (q.device == k_pages.device == v_pages.device == block_table.device == seqlens.device):
+        raise ValueError("q, the pools, block_table and seqlens must be on one device")
+    if tuple(k_pages.shape) != tuple(v_pages.shape) or k_pages.shape[3] != d:
+        raise ValueError(f"k_pages and v_pages must both be [P][page_size][Hkv][{d}]")
+    if block_table.shape[0] != B or tuple(seqlens.shape) != (B,):
+        raise ValueError(f"block_table must be [{B}][max_pages] and seqlens [{B}]")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     n = int(num_splits) or fa_decode_num_splits(B, Hq, Hkv, T, max_pages * page_size, True, device=q.device)
     ws, ws_bytes = _workspace(B, Hq, T, d, n, q.device, workspace)
-    o = torch.empty_like(q) if out is None else out
-    if lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    o = _out(out, "out", q.shape, torch.bfloat16, q)
+    lse = _out(lse, "lse", (B, Hq, T), torch.float32, q)
     st = lib().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), _ptr(o),
                                _ptr(lse), B, Hq, Hkv, T, max_pages, page_size, P, d, scale, int(causal),
                                int(num_splits), _ptr(ws), ws_bytes, _stream(q))

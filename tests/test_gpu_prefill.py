@@ -172,3 +172,33 @@ def test_api_errors_raise():
     k = torch.zeros(1, 2, 8, 96, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(fa.FAError):
         fa.fa_fwd(q, k, k)
+
+
+def test_binding_rejects_mismatched_tensors():
+    """The library takes every size from q and k and writes outputs through bare
+    pointers, so the binding refuses, before any launch, tensors whose shapes would
+    let it read or write past an allocation."""
+    fa = _fa()
+    bf = dict(dtype=torch.bfloat16, device=DEV)
+    q = torch.zeros(2, 4, 64, 64, **bf)
+    k = torch.zeros(2, 2, 96, 64, **bf)
+    bad = [
+        lambda: fa.fa_fwd(q, k, torch.zeros(2, 2, 48, 64, **bf)),                     # v shorter than k
+        lambda: fa.fa_fwd(torch.zeros(1, 4, 64, 64, **bf), k, k),                       # batch differs
+        lambda: fa.fa_fwd(q, k, k, out=torch.zeros(2, 4, 32, 64, **bf)),               # out too small
+        lambda: fa.fa_fwd(q, k, k, out=torch.zeros(2, 4, 64, 64, dtype=torch.float32, device=DEV)),
+        lambda: fa.fa_fwd(q, k, k, lse=torch.zeros(2, 4, 63, device=DEV)),              # lse too small
+        lambda: fa.fa_fwd(q, k, k, out=torch.zeros(2, 4, 64, 128, **bf)[..., ::2]),     # strided out
+        lambda: fa.fa_decode_splitkv(q[:, :, :1], k, k, out=torch.zeros(2, 4, 2, 64, **bf)),
+        lambda: fa.fa_fwd_kv_outer(q, k, torch.zeros(2, 2, 96, 32, **bf)),
+        lambda: fa.fa_bwd(q, k, k, q, torch.zeros(2, 4, 64, device=DEV), torch.zeros(2, 4, 32, 64, **bf)),
+        lambda: fa.fa_bwd(q, k, k, q, torch.zeros(2, 4, 64, device=DEV), q, dk=torch.zeros(2, 2, 95, 64, **bf)),
+        lambda: fa.fa_decode_paged(q[:, :, :1], torch.zeros(10, 16, 2, 64, **bf), torch.zeros(10, 16, 2, 64, **bf),
+                                   torch.zeros(3, 5, dtype=torch.int32, device=DEV),
+                                   torch.zeros(2, dtype=torch.int32, device=DEV)),        # table rows != batch
+    ]
+    for i, call in enumerate(bad):
+        with pytest.raises(ValueError):
+            call()
+    st, word = fa.fa_get_last_device_error()
+    assert st == 0, hex(word)

@@ -211,6 +211,11 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // A launch that follows this one on the stream as a programmatic dependent (the next
+  // call of this kernel, or the key split's merge) may start its CTAs as SMs free up;
+  // it reads nothing of ours before its griddepcontrol.wait, which returns only once
+  // this grid has completed and its stores are visible.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -229,6 +234,10 @@ __global__ void __launch_bounds__(384, 1)
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+  // This grid may itself have started before the work ahead of it on the stream
+  // completed (it launches as a programmatic dependent): nothing global is read or
+  // written before that work is complete and visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // paged: rank the sequences by key count, longest first (ties by index)
   int* order_smem = reinterpret_cast<int*>(smem + C::OFF_ORDER);
   const int* order = nullptr;
@@ -759,10 +768,22 @@ template <int D, bool PAGED, bool SPLIT = false>
 static int launch_pf(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PfParams& p, int grid,
                      cudaStream_t stream) {
   auto kfn = prefill_tc_kernel<D, PAGED, SPLIT>;
-  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM) != cudaSuccess)
+  const int smem = PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return FA_ERR_CUDA;
-  kfn<<<grid, PfCfg<D>::THREADS, PAGED ? PfCfg<D>::SMEM_PAGED : PfCfg<D>::SMEM, stream>>>(tq, tk, tv, p);
+  // a programmatic dependent of the previous launch on the stream: the CTAs' setup
+  // (barriers, TMEM) overlaps that launch's tail; the kernel waits before any global access
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(PfCfg<D>::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kfn, tq, tk, tv, p) != cudaSuccess) return FA_ERR_CUDA;
   return launch_status();
 }
 

@@ -107,6 +107,10 @@ __global__ void __launch_bounds__(160, PAGED ? 2 : 1)
   const int b = bh / p.Hkv;
   const int kvh = bh % p.Hkv;
 
+  // launched as a programmatic dependent of the previous launch on the stream (for a
+  // decode loop, the previous step's merge, which still reads the partials this grid
+  // overwrites): nothing global is read or written before that launch has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int S_b = p.S;
   if (PAGED) S_b = max(0, min(p.seqlens[b], p.max_pages * 16));
   const int per = (S_b + p.num_splits - 1) / p.num_splits;
@@ -444,6 +448,9 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float* __restrict_
   // launched as a programmatic dependent of the split kernel: wait until that grid
   // has finished and its partials are visible (a no-op for a plain launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next launch on the stream may start now; it waits for this grid before it
+  // touches anything (the next decode step overwrites the partials read here)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -564,8 +571,19 @@ static int launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const D
   auto kfn = decode_kernel<D, ST, PAGED>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  dim3 grid(nsplit, nbh);
-  kfn<<<grid, C::THREADS, C::SMEM, stream>>>(tk, tv, p);
+  // a programmatic dependent of the previous launch on the stream: the launch and the
+  // CTAs' start overlap that launch's tail; the kernel waits before any global access
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nsplit, nbh);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kfn, tk, tv, p) != cudaSuccess) return FA_ERR_CUDA;
   return launch_status();
 }
 

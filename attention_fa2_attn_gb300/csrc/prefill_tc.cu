@@ -212,10 +212,11 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x & 31;
 
   // A launch that follows this one on the stream as a programmatic dependent (the next
-  // call of this kernel, or the key split's merge) may start its CTAs as SMs free up;
-  // it reads nothing of ours before its griddepcontrol.wait, which returns only once
-  // this grid has completed and its stores are visible.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // call of this kernel) may start its CTAs as SMs free up; it reads nothing of ours
+  // before its griddepcontrol.wait, which returns only once this grid has completed and
+  // its stores are visible. The key split is followed by its merge, whose thousands of
+  // small blocks would only sit waiting on the SMs; it launches at this grid's end.
+  if constexpr (!SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);

@@ -100,3 +100,31 @@ def test_concurrent_streams_match_plain_calls():
         _assert_same(a, b, f"stream {i}")
     st, word = fa.fa_get_last_device_error()
     assert st == 0, hex(word)
+
+
+def test_launch_after_event_wait_sees_the_copied_inputs():
+    """A call that follows another call on its stream launches as a programmatic
+    dependent of it, but an event wait between them (inputs copied on another
+    stream) must still hold it back: the 201 MB host-to-device copy below takes
+    about a millisecond, far longer than the short call ahead on the stream, so a
+    launch that ignored the event would read the zero-filled buffers."""
+    fa = _fa()
+    shape_q, shape_kv = (4, 16, 4096, 128), (4, 16, 4096, 128)
+    qh, kh, vh = (fi.randn(s, 1500 + i).pin_memory() for i, s in enumerate((shape_q, shape_kv, shape_kv)))
+    q1, k1, v1 = (torch.zeros(s, dtype=torch.bfloat16, device=DEV) for s in (shape_q, shape_kv, shape_kv))
+    tq, tk, tv = (x.to(DEV) for x in fi.qkv(1, 1, 1, 64, 64, 128, 1503))
+    copy_stream, work_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    copied = torch.cuda.Event()
+    with torch.cuda.stream(copy_stream):
+        for dst, src in ((q1, qh), (k1, kh), (v1, vh)):
+            dst.copy_(src, non_blocking=True)
+        copied.record(copy_stream)
+    with torch.cuda.stream(work_stream):
+        fa.fa_fwd(tq, tk, tv)  # a short call ahead on the stream
+        work_stream.wait_event(copied)
+        o, lse = fa.fa_fwd(q1, k1, v1)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = fa.fa_fwd(q1, k1, v1)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)

@@ -30,6 +30,13 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream). Argument errors are returned synchronously, before
  *     anything is launched; FA_ERR_CUDA reports a failed launch.
+ *   - The prefill, decode and backward kernels launch as programmatic
+ *     dependents of the launch before them on `stream` and may start while
+ *     it finishes; each waits (griddepcontrol.wait) before its first access
+ *     to global memory, so stream order holds for every input and output.
+ *     The prefill (unsplit) and the LSE merge also let the next launch on the
+ *     stream start early; a kernel of the caller's launched that way after
+ *     them must likewise wait before reading their outputs.
  *   - Kernels never trap. Every wait inside a kernel is bounded; a wait that
  *     runs out, or a bounds check that fails (paged block-table entries),
  *     records a code in a device-side error word and the kernel returns.

@@ -39,31 +39,42 @@ namespace fa {
 // ---------------------------------------------------------------------------
 // Per query row, into the row-vector workspace [2][B*Hq][T_pad]: -D = -rowsum(dO * O)
 // (plane 0) and -lse * log2(e), the row's LSE in base 2 negated (plane 1; -inf for
-// a row with no visible key, so that its P is 0). A group of d / 8 lanes takes a
-// row, one 16-byte load of O and of dO per lane (HBM-bound: every byte of O and dO
-// is read once). Every block lets the main kernel launch as its programmatic
-// dependent at once; that kernel waits (griddepcontrol.wait) only where it reads
-// these values.
-// ---------------------------------------------------------------------------
+// a row with no visible key, so that its P is 0). A group of d / 16 lanes takes a
+// row, 32 bytes of O and of dO per lane in four 16-byte loads issued together
+// (HBM-bound: every byte of O and dO is read once). The kernel launches as a
+// programmatic dependent of the launch before it on the stream (for a training loop,
+// the previous backward's main grid) and waits before it reads anything; every block
+// lets the main kernel launch as its own programmatic dependent at once, and that
+// kernel waits (griddepcontrol.wait) only where it reads these values.
 __global__ void __launch_bounds__(256) bwd_rowsum_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ d_o,
                                                          const float* __restrict__ lse, float* __restrict__ vecs,
                                                          long long rows, int T, int T_pad, int d) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int lanes = d / 8;  // 16 (d = 128) or 8 (d = 64): a power of two dividing 32
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the work ahead on the stream is complete
+  const int lanes = d / 16;  // 8 (d = 128) or 4 (d = 64): a power of two dividing 32
   const int sub = threadIdx.x & (lanes - 1);
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / lanes;
   float acc = 0.f;
   if (row < rows) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + row * d + sub * 8);
-    const uint4 g = *reinterpret_cast<const uint4*>(d_o + row * d + sub * 8);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+    const uint4* pa = reinterpret_cast<const uint4*>(o + row * d + sub * 16);
+    const uint4* pg = reinterpret_cast<const uint4*>(d_o + row * d + sub * 16);
+    // streaming loads: this pass reads each byte once
+    uint4 a[2], g[2];
+    a[0] = __ldcs(pa);
+    a[1] = __ldcs(pa + 1);
+    g[0] = __ldcs(pg);
+    g[1] = __ldcs(pg + 1);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 x = __bfloat1622float2(a2[k]);
-      const float2 y = __bfloat1622float2(g2[k]);
-      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    for (int h = 0; h < 2; ++h) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[h]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[h]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 x = __bfloat1622float2(a2[k]);
+        const float2 y = __bfloat1622float2(g2[k]);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+      }
     }
   }
   for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -884,6 +895,9 @@ __global__ void __launch_bounds__(320, 1)
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmVec, const BwParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the next launch on the stream (for a training loop, the next backward's row pass)
+  // may start as SMs free up; it waits for this grid before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment and the layout has no slack
     if (threadIdx.x == 0) record_error(p.err, FA_ERR_BOUNDS, SITE_BW_SMEM);
     return;
@@ -983,9 +997,24 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
       return FA_ERR_CUDA;
   }
   const long long rows = static_cast<long long>(B) * Hq * T;
-  const long long rows_per_block = 256 / (d / 8);
-  bwd_rowsum_kernel<<<static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, vecs, rows, T, T_pad, d);
+  const long long rows_per_block = 256 / (d / 16);
+  {
+    // a programmatic dependent of the launch before it on the stream (it waits before
+    // reading anything)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, bwd_rowsum_kernel, static_cast<const __nv_bfloat16*>(o),
+                           static_cast<const __nv_bfloat16*>(d_o), lse, vecs, rows, T, T_pad, d) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
   BwParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);

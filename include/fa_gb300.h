@@ -34,9 +34,10 @@
  *     dependents of the launch before them on `stream` and may start while
  *     it finishes; each waits (griddepcontrol.wait) before its first access
  *     to global memory, so stream order holds for every input and output.
- *     The unsplit prefill, the decode kernel and the LSE merge also let the
- *     next launch on the stream start early; a kernel of the caller's launched
- *     that way after them must likewise wait before reading their outputs.
+ *     The unsplit prefill, the decode kernel, the LSE merge and the backward's
+ *     main grid also let the next launch on the stream start early; a kernel of
+ *     the caller's launched that way after them must likewise wait before
+ *     reading their outputs.
  *   - Kernels never trap. Every wait inside a kernel is bounded; a wait that
  *     runs out, or a bounds check that fails (paged block-table entries),
  *     records a code in a device-side error word and the kernel returns.

@@ -40,11 +40,21 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
 
 
+def _on_current_device(t: torch.Tensor):
+    """The library launches on the current CUDA device; tensors elsewhere would be read
+    through another device's pointers."""
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"the tensors are on {t.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device)")
+
+
 def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
-    """q [B][Hq][T][d], k and v [B][Hkv][S][d] on one device. The library takes every
-    size from q and k, so v must match k exactly and q must share B and d."""
+    """q [B][Hq][T][d], k and v [B][Hkv][S][d] on one device, the current one. The
+    library takes every size from q and k, so v must match k exactly and q must share
+    B and d."""
     if not (q.device == k.device == v.device):
         raise ValueError("q, k and v must be on one device")
+    _on_current_device(q)
     if tuple(k.shape) != tuple(v.shape):
         raise ValueError(f"k and v must have one shape, got {tuple(k.shape)} and {tuple(v.shape)}")
     if q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
@@ -237,8 +247,9 @@ def fa_lse_merge(o_part, lse_part):
     _need(o_part, "o_part", torch.float32, 3)
     _need(lse_part, "lse_part", torch.float32, 2)
     n, rows, d = o_part.shape
-    if tuple(lse_part.shape) != (n, rows):
-        raise ValueError("lse_part must be [n][rows]")
+    if tuple(lse_part.shape) != (n, rows) or lse_part.device != o_part.device:
+        raise ValueError("lse_part must be [n][rows] on o_part's device")
+    _on_current_device(o_part)
     o = torch.empty((rows, d), dtype=torch.bfloat16, device=o_part.device)
     lse = torch.empty((rows,), dtype=torch.float32, device=o_part.device)
     st = lib().fa_lse_merge(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), n, rows, d, _stream(o_part))
@@ -259,6 +270,7 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, causal: bool = Tr
     max_pages = block_table.shape[1]
     if not (q.device == k_pages.device == v_pages.device == block_table.device == seqlens.device):
         raise ValueError("q, the pools, block_table and seqlens must be on one device")
+    _on_current_device(q)
     if tuple(k_pages.shape) != tuple(v_pages.shape) or k_pages.shape[3] != d:
         raise ValueError(f"k_pages and v_pages must both be [P][page_size][Hkv][{d}]")
     if block_table.shape[0] != B or tuple(seqlens.shape) != (B,):
